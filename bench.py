@@ -1,0 +1,466 @@
+"""Benchmark of the W4A16 group-quantized GEMM on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline workload (one step): the decode set -- one token (M=1) through the
+four INT4 projections of a ~4B-decoder layer, qkv 2560x4096, o_proj 4096x2560,
+gate_up 2560x19456, down 9728x2560, group 128 ("Quantize the Target, Quantize
+the Drafter", pith.science review: INT4 target and drafter, group size 128).
+Metric: effective HBM GB/s = algorithmic bytes / time, with
+bytes = K*N/2 + (K/128)*N*2.5 + 2*M*K + 2*M*N per GEMM.  Inputs are seeded
+synthetic tensors with the workload's distributions (w4a16_inputs).
+
+L2: the step rotates through 8 distinct copies of the packed weights (398 MB,
+more than twice the 129 MB L2), so every step streams its weights from HBM,
+as a forward pass through 8 different layers would.
+
+Also printed in the same JSON line: the verify set (M=16) in GB/s, prefill
+(M=2048) in TFLOP/s, each GEMM alone, the roofline of the dominant kernel,
+the end-to-end number through the public API with host buffers, and the CPU
+oracle timed on this host.  `--impl reference` times the CPU oracle (the only
+reference implementation of this path) on the same metric.
+
+Multi-GPU: the GEMM needs no exchange, so N GPUs run N independent replicas
+(weak scaling); value = bytes of all ranks / slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import w4a16_inputs as wi  # noqa: E402
+
+METRIC = "W4A16 GEMM effective HBM GB/s (M=1,16) and TFLOP/s (M≥2048), % of roofline"
+COPIES = 8
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def gemm_bytes(M, K, N, group=128):
+    G = K // group
+    return K * N // 2 + G * N * 2 + G * N // 2 + 2 * M * K + 2 * M * N
+
+
+def gemm_flops(M, K, N):
+    return 2 * M * N * K
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "int4_weight_only_gemm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel sources
+    still match the ones profiled; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    e = d.get(kernel_key)
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_step")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the GPU works."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    cfg_name, seed, items = wi.CONFIGS[1]
+    probs = [wi.generate_named(s, M, seed) for (s, M) in items]
+    total_steps = args.steps + args.warmup
+    # per-step sample: a column window of every projection, sized so that the
+    # whole run stays near `budget` seconds of CPU work
+    budget = 60.0
+    full_bytes = sum(gemm_bytes(p.M, p.K, p.N) for p in probs)
+    t0 = time.perf_counter()
+    oracle.gemm(probs[0].x, probs[0].qweight[:, :256].copy(), probs[0].scales[:, :256].copy(),
+                probs[0].qzeros[:, :32].copy())
+    per_col = (time.perf_counter() - t0) / 256 * (full_bytes / gemm_bytes(1, probs[0].K, probs[0].N)) / probs[0].N
+    frac = min(1.0, max(budget / max(total_steps, 1) / max(per_col * probs[0].N, 1e-9), 0.0))
+    windows = []
+    for p in probs:
+        w = max(8, int(p.N * frac) // 8 * 8)
+        w = min(w, p.N)
+        sl = []
+        for i in range(4):
+            c0 = ((p.N - w) * i // 4) // 8 * 8
+            sl.append((p.x, np.ascontiguousarray(p.qweight[:, c0:c0 + w]),
+                       np.ascontiguousarray(p.scales[:, c0:c0 + w]),
+                       np.ascontiguousarray(p.qzeros[:, c0 // 8:(c0 + w) // 8]), p.M, p.K, w))
+        windows.append(sl)
+    step_bytes = sum(gemm_bytes(sl[0][4], sl[0][5], sl[0][6]) for sl in windows)
+    threads = oracle.max_threads()
+    for i in range(args.warmup):
+        for sl in windows:
+            a = sl[i % 4]
+            oracle.gemm(a[0], a[1], a[2], a[3])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        for sl in windows:
+            a = sl[i % 4]
+            oracle.gemm(a[0], a[1], a[2], a[3])
+    dt = time.perf_counter() - t0
+    value = step_bytes * args.steps / dt / 1e9
+    cols = [(items[j][0], windows[j][0][6], p.N) for j, p in enumerate(probs)]
+    sample = (f"decode set M=1, each step a column window of every projection "
+              f"({', '.join(f'{s} {w}/{n}' for s, w, n in cols)} columns), full K")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / max(args.steps, 1) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode_m1: qkv 2560x4096, o_proj 4096x2560, gate_up 2560x19456, "
+                               "down 9728x2560, M=1, group 128", "implementation": "CPU oracle (fp64 triple loop)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class Workload:
+    """A list of GEMMs resident on the GPU with COPIES weight copies each."""
+
+    def __init__(self, w, torch, items, seed, copies, device):
+        self.w, self.torch = w, torch
+        self.gemms = []
+        for (shape, M) in items:
+            p = wi.generate_named(shape, M, seed)
+            x, qw, sc, qz = w.to_device(p, device)
+            qd = w.w4a16_pack(qw)
+            qds = [qd] + [qd.clone() for _ in range(copies - 1)]
+            del qw
+            y = torch.empty((M, p.N), dtype=torch.bfloat16, device=device)
+            need = w.w4a16_workspace_bytes(M, p.N, p.K)
+            ws = w.new_workspace(need, device)
+            self.gemms.append(dict(p=p, shape=shape, M=M, K=p.K, N=p.N, x=x, qds=qds, sc=sc, qz=qz, y=y, ws=ws,
+                                   ws_bytes=ws.numel()))
+        self.copies = copies
+        self.bytes = sum(gemm_bytes(g["M"], g["K"], g["N"]) for g in self.gemms)
+        self.flops = sum(gemm_flops(g["M"], g["K"], g["N"]) for g in self.gemms)
+
+    def launch_step(self, copy, stream_ptr, only=None):
+        w = self.w
+        n = 0
+        for i, g in enumerate(self.gemms):
+            if only is not None and i != only:
+                continue
+            st = w.w4a16_gemm_raw(g["x"].data_ptr(), g["qds"][copy].data_ptr(), g["sc"].data_ptr(),
+                                  g["qz"].data_ptr(), g["M"], g["N"], g["K"], 128, g["y"].data_ptr(),
+                                  g["ws"].data_ptr(), g["ws_bytes"], 0, stream_ptr)
+            if st != 0:
+                raise RuntimeError(f"w4a16_gemm failed: {w.w4a16_status_str(st)}")
+            n += 1
+        return n
+
+    def graphs(self, only=None):
+        """One graph per weight copy (a step each) and one for the whole rotation."""
+        torch = self.torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for c in range(self.copies):  # warm-up outside capture
+                self.launch_step(c, s.cuda_stream, only)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        per_step = []
+        for c in range(self.copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.launch_step(c, torch.cuda.current_stream().cuda_stream, only)
+            per_step.append(g)
+        rot = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(rot):
+            for c in range(self.copies):
+                self.launch_step(c, torch.cuda.current_stream().cuda_stream, only)
+        torch.cuda.synchronize()
+        return per_step, rot
+
+
+def replay_steps(per_step, rot, copies, start, count):
+    """Replays exactly `count` steps beginning at step index `start`."""
+    i = start
+    end = start + count
+    while i < end and i % copies:
+        per_step[i % copies].replay()
+        i += 1
+    while i + copies <= end:
+        rot.replay()
+        i += copies
+    while i < end:
+        per_step[i % copies].replay()
+        i += 1
+
+
+def time_graph_steps(torch, per_step, rot, copies, steps, warmup, barrier=None):
+    replay_steps(per_step, rot, copies, 0, warmup)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    replay_steps(per_step, rot, copies, warmup, steps)
+    e1.record()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return e0.elapsed_time(e1)  # ms
+
+
+def measure_e2e(w, torch, wl, steps):
+    """Through the public binding with host buffers: per step, pinned-host
+    activations go to the device, the four GEMMs run, the outputs come back to
+    pinned host memory, and the host waits for them."""
+    hx = [g["x"].cpu().pin_memory() for g in wl.gemms]
+    hy = [torch.empty_like(g["y"], device="cpu").pin_memory() for g in wl.gemms]
+    dx = [torch.empty_like(g["x"]) for g in wl.gemms]
+    h2d = sum(t.numel() * 2 for t in hx)
+    d2h = sum(t.numel() * 2 for t in hy)
+    stream = torch.cuda.current_stream()
+
+    def one(i):
+        c = i % wl.copies
+        for j, g in enumerate(wl.gemms):
+            dx[j].copy_(hx[j], non_blocking=True)
+            w.w4a16_gemm(dx[j], g["qds"][c], g["sc"], g["qz"], out=g["y"], workspace=g["ws"])
+            hy[j].copy_(g["y"], non_blocking=True)
+        stream.synchronize()
+
+    for i in range(min(20, steps)):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    dt = time.perf_counter() - t0
+    return wl.bytes * steps / dt / 1e9, h2d, d2h, dt / steps * 1e3
+
+
+def cpu_baseline(min_seconds=8.0):
+    import oracle
+    _, seed, items = wi.CONFIGS[1]
+    probs = [wi.generate_named(s, M, seed) for (s, M) in items]
+    step_bytes = sum(gemm_bytes(p.M, p.K, p.N) for p in probs)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        for p in probs:
+            oracle.gemm(p.x, p.qweight, p.scales, p.qzeros)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or n >= 200:
+            break
+    return {"value": step_bytes * n / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"the full decode set (4 projections, M=1) repeated {n} times, {dt:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=1000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the M=16 / M=2048 / per-GEMM extras")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer measurement")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import int4_weight_only_gemm_gb300 as w
+    w.load_library()  # raises if the CUDA library is missing: there is no fallback
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+
+    _, seed1, items1 = wi.CONFIGS[1]
+    wl = Workload(w, torch, items1, seed1, COPIES, device)
+    per_step, rot = wl.graphs()
+    launches0 = w.w4a16_launch_count()
+    with ClockSampler(local_rank) as clk:
+        ms = time_graph_steps(torch, per_step, rot, COPIES, args.steps, args.warmup, barrier)
+    clocks = clk.summary()
+    launches_in_graphs = len(wl.gemms) * args.steps  # graph replays do not pass through the library
+    if dist is not None:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = wl.bytes * args.steps * world / (ms / 1e3) / 1e9
+
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        # each projection alone (graph of the 8-copy rotation of that GEMM)
+        per = {}
+        for i, g in enumerate(wl.gemms):
+            ps, rt = wl.graphs(only=i)
+            n = max(200, min(args.steps, 20000))
+            t_ms = time_graph_steps(torch, ps, rt, COPIES, n, 50)
+            b = gemm_bytes(g["M"], g["K"], g["N"])
+            per[g["shape"]] = {"us": t_ms / n * 1e3, "GB/s": b * n / (t_ms / 1e3) / 1e9,
+                               "frac": b * n / (t_ms / 1e3) / 1e9 / hbm}
+        extra["decode_m1_per_gemm"] = per
+        for cfg, unit in ((2, "GB/s"), (3, "TFLOP/s")):
+            name, seed, items = wi.CONFIGS[cfg]
+            copies = COPIES if cfg == 2 else 2
+            wl2 = Workload(w, torch, items, seed, copies, device)
+            ps, rt = wl2.graphs()
+            n = 4000 if cfg == 2 else 40
+            t_ms = time_graph_steps(torch, ps, rt, copies, n, 10)
+            if unit == "GB/s":
+                v = wl2.bytes * n / (t_ms / 1e3) / 1e9
+                frac = v / hbm
+            else:
+                v = wl2.flops * n / (t_ms / 1e3) / 1e12
+                frac = v / bf16_peak
+            extra[name] = {"value": v, "unit": unit, "frac": frac, "ms_per_step": t_ms / n,
+                           "workload": ", ".join(f"{s} M={M}" for s, M in items)}
+            del wl2, ps, rt
+            torch.cuda.empty_cache()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_v, h2d, d2h, e2e_ms = measure_e2e(w, torch, wl, min(2000, max(50, args.steps // 10)))
+        e2e = {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms, "api": "int4_weight_only_gemm_gb300.w4a16_gemm (C ABI w4a16_gemm_path)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline()
+
+    if rank == 0:
+        achieved = wl.bytes / (ms_step / 1e3) / 1e9
+        traffic = profiled_traffic("gemv_decode_m1_step")
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "decode_m1: one token through qkv 2560x4096, o_proj 4096x2560, "
+                                   "gate_up 2560x19456, down 9728x2560; group 128; int4 weights, bf16 x/y",
+                       "global_batch": 1, "parallelism": f"replicas x{world}",
+                       "l2": f"rotating {COPIES} weight copies ({COPIES * wl.bytes / 1e6:.0f} MB > 2x L2)",
+                       "bytes_per_step": wl.bytes, "launch": "CUDA graph of the 8-copy rotation"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": traffic,
+                         "kernel": "gemv_kernel<1> (all four GEMMs of the step)",
+                         "peak_source": f"{peak_src} hbm_gbs"},
+            "e2e": e2e,
+            "gpu_launches": launches_in_graphs,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+/*
+ * w4a16.h -- C ABI of the W4A16 group-quantized GEMM library for GB300 (sm_103a).
+ *
+ *     y[m][n] = sum_k x[m][k] * (q[k][n] - z[k/g][n]) * s[k/g][n]
+ *
+ * This is the linear layer of the INT4 models in "Quantize the Target,
+ * Quantize the Drafter: Efficient Inference with Qwen3.5-4B": an AWQ INT4
+ * target whose per-group scales are kept and whose weights are re-packed on
+ * the same grid (pith.science review, referee report summary), and a GPTQ
+ * INT4 drafter with group size 128 (same review, "Assumptions & free
+ * parameters").  Both run it on every decode step and on every verify of a
+ * 16-token draft block (DFlash block size 16, same section).
+ *
+ * The pages give no interface, layout or zero-point convention.  Readings:
+ *   - x: bfloat16, row-major [M][K].  y: bfloat16, row-major [M][N], fully
+ *     overwritten (no bias, no accumulate), rounded to nearest even.
+ *   - qweight (canonical): uint32 [K/8][N]; bits 4i..4i+3 of qweight[j][n]
+ *     hold the unsigned 4-bit code of row k = 8j+i.
+ *   - scales: IEEE binary16, row-major [K/g][N].
+ *   - qzeros: uint32 [K/g][N/8]; bits 4i..4i+3 of qzeros[gi][c] hold the
+ *     unsigned 4-bit zero point of column n = 8c+i (packed along N because
+ *     K/g is 20 or 76 for some layer shapes, which 8 does not divide).
+ *   - weight = (code - zero) * scale, zero used as stored; groups are
+ *     contiguous along K (group of row k is k/g).  g = 128 is supported.
+ *
+ * Device layout (output of w4a16_pack, input of w4a16_gemm): the same
+ * K*N/2 bytes, re-ordered into column tiles of 128 (the last tile is
+ * W = N - 128*nb wide) and K blocks of 128 rows:
+ *   tile nb starts at word 128*16*(K/128)*nb; its block kb at + kb*W*16;
+ *   inside a block, word (c*W + t)*4 + j (c, j in 0..3, t < W) holds column
+ *   n = 128*nb + t, rows k = 128*kb + 8*(4c + j) + r for r = 0..7;
+ *   inside that word, nibble position p holds row offset r = 2p (p < 4) or
+ *   r = 2(p-4) + 1 (p >= 4), so that one mask-and-or turns a word shifted by
+ *   4p into a bfloat16 pair of rows (2p, 2p+1).
+ * A 16-row-by-128-column slab is thus 2 KB contiguous, and a tile's whole K
+ * range is contiguous, which is what the kernels stream.
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers owned by the caller; the library never
+ *     allocates, frees or retains them.  x, y, qweight, qweight_dev,
+ *     scales, qzeros and the workspace must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream); they
+ *     return after launching.  Arguments are validated before any launch;
+ *     on a non-zero return nothing was launched (W4A16_ECUDA: a launch or a
+ *     runtime query failed).  Nothing throws across the ABI.
+ *   - y must not overlap any input.  Calls are thread-safe when they use
+ *     different workspaces; two calls that may run at the same time on the
+ *     GPU must not share one workspace.
+ *   - Requirements: M >= 1, N >= 8, N % 8 == 0, K >= 128, K % 128 == 0,
+ *     group == 128; M, N, K < 2^31 and K*N/8 < 2^31.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared opaquely so that this header does not
+ * need the CUDA headers. */
+typedef struct CUstream_st *w4a16_stream_t;
+
+typedef enum {
+    W4A16_OK = 0,
+    W4A16_EINVAL = -1,        /* null pointer, bad size, or overlapping output */
+    W4A16_EALIGN = -2,        /* a pointer is not 16-byte aligned */
+    W4A16_EUNSUPPORTED = -3,  /* group != 128, or K / N outside the supported set */
+    W4A16_ECUDA = -4,         /* a CUDA runtime call or kernel launch failed */
+    W4A16_ETIMEOUT = -5,      /* a bounded device-side wait gave up (see below) */
+    W4A16_EWORKSPACE = -6     /* workspace missing, too small or misaligned */
+} w4a16_status;
+
+/* Kernel choice for w4a16_gemm_path (AUTO picks per M from a measured table). */
+typedef enum {
+    W4A16_PATH_AUTO = 0,
+    W4A16_PATH_GEMV = 1,      /* CUDA-core split-K GEMV, M <= 8 */
+    W4A16_PATH_TC = 2         /* tcgen05 tensor-core GEMM, any M */
+} w4a16_path;
+
+/*
+ * Canonical qweight [K/8][N] -> device layout (same size, documented above).
+ * Integer-only and exact; `qweight_dev` must not overlap `qweight`.
+ * Grid-preserving packing: codes keep their values, only their order changes
+ * (the pages' "re-packs onto the same grid", pith.science review summary).
+ */
+int w4a16_pack(const uint32_t *qweight, uint32_t *qweight_dev, int K, int N,
+               w4a16_stream_t stream);
+
+/* Exact inverse of w4a16_pack: device layout -> canonical [K/8][N]. */
+int w4a16_unpack(const uint32_t *qweight_dev, uint32_t *qweight, int K, int N,
+                 w4a16_stream_t stream);
+
+/*
+ * Bytes of workspace w4a16_gemm needs for this problem on the current device
+ * (0 when the chosen plan needs none).  Returns 0 for invalid arguments too.
+ * The workspace carries per-tile arrival counters (its first 64 KB) and
+ * split-K partial sums (the rest).  It must be zero-filled once before its
+ * first use; every call leaves the counter area at zero again, so one
+ * workspace serves any sequence of calls, whatever their shapes.
+ */
+size_t w4a16_workspace_bytes(int M, int N, int K, int group);
+
+/* Largest workspace any problem with these N, K and M <= max_M can need on
+ * the current device. */
+size_t w4a16_workspace_bytes_max(int max_M, int N, int K, int group);
+
+/*
+ * Registers a caller-owned workspace for the current device, used by
+ * w4a16_gemm (NULL, 0 unregisters).  The library keeps only the pointer.
+ */
+int w4a16_set_workspace(void *workspace, size_t bytes);
+
+/*
+ * y = x . dequant(qweight_dev, scales, qzeros), kernel chosen per M.
+ * Uses the workspace registered for the current device when the plan needs
+ * one (W4A16_EWORKSPACE if it is missing or too small).
+ */
+int w4a16_gemm(const void *x, const uint32_t *qweight_dev, const void *scales,
+               const uint32_t *qzeros, int M, int N, int K, int group, void *y,
+               w4a16_stream_t stream);
+
+/* As w4a16_gemm, with an explicit workspace (may be NULL when
+ * w4a16_workspace_bytes returns 0). */
+int w4a16_gemm_ws(const void *x, const uint32_t *qweight_dev, const void *scales,
+                  const uint32_t *qzeros, int M, int N, int K, int group, void *y,
+                  void *workspace, size_t workspace_bytes, w4a16_stream_t stream);
+
+/* As w4a16_gemm_ws with an explicit kernel choice (for tests and tuning).
+ * W4A16_EUNSUPPORTED when the path cannot run this M. */
+int w4a16_gemm_path(int path, const void *x, const uint32_t *qweight_dev,
+                    const void *scales, const uint32_t *qzeros, int M, int N, int K,
+                    int group, void *y, void *workspace, size_t workspace_bytes,
+                    w4a16_stream_t stream);
+
+/* Workspace bytes for a given path (0 if none); 0 for unsupported input. */
+size_t w4a16_workspace_bytes_path(int path, int M, int N, int K, int group);
+
+/* The path AUTO takes for this problem on the current device (or < 0). */
+int w4a16_auto_path(int M, int N, int K, int group);
+
+/* Static string for a status code. */
+const char *w4a16_status_str(int status);
+
+/*
+ * Synchronizes `stream`, then returns and clears the device-side status word
+ * of the current device: W4A16_OK, or W4A16_ETIMEOUT when a kernel's bounded
+ * wait on a barrier gave up (its output is then undefined, the context stays
+ * usable).  W4A16_ECUDA if the synchronization itself failed.
+ */
+int w4a16_last_device_status(w4a16_stream_t stream);
+
+/*
+ * Failure-detection self-test.  Launches one thread that waits on a shared-
+ * memory barrier which nothing ever completes, through the same bounded wait
+ * the GEMM pipelines use, with a limit of `wait_ns` nanoseconds (1e3..1e9).
+ * Expected outcome: w4a16_last_device_status(stream) returns W4A16_ETIMEOUT
+ * and the context stays usable.  W4A16_EINVAL for a limit out of range.
+ */
+int w4a16_selftest_wait_timeout(long long wait_ns, w4a16_stream_t stream);
+
+/* Number of kernel launches the library has issued in this process. */
+uint64_t w4a16_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

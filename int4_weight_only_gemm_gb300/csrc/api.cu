@@ -1,0 +1,259 @@
+// C ABI of the W4A16 library: argument checks, per-M kernel choice,
+// workspace bookkeeping and status reporting.  See include/w4a16.h.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace w4a16 {
+
+
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_mu;
+int g_sms[kMaxDevices];
+void* g_ws[kMaxDevices];
+size_t g_ws_bytes[kMaxDevices];
+
+int current_device() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+    return d;
+}
+
+int device_sms(int dev) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sms[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        g_sms[dev] = v;
+    }
+    return g_sms[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+int check_kn(int N, int K) {
+    if (N < 8 || K < 128 || N % 8 != 0) return W4A16_EINVAL;
+    if (K % 128 != 0) return W4A16_EUNSUPPORTED;
+    if ((long long)(K / 8) * N >= (1ll << 31)) return W4A16_EUNSUPPORTED;
+    return W4A16_OK;
+}
+
+int check_gemm(const void* x, const uint32_t* qd, const void* scales, const uint32_t* qzeros, int M, int N, int K,
+               int group, void* y) {
+    if (!x || !qd || !scales || !qzeros || !y) return W4A16_EINVAL;
+    if (M < 1) return W4A16_EINVAL;
+    if (group != 128) return W4A16_EUNSUPPORTED;
+    int st = check_kn(N, K);
+    if (st != W4A16_OK) return st;
+    if (!aligned16(x) || !aligned16(qd) || !aligned16(y) || !aligned16(scales) || !aligned16(qzeros))
+        return W4A16_EALIGN;
+    const size_t ybytes = (size_t)M * N * 2;
+    const int G = K / group;
+    if (overlaps(y, ybytes, x, (size_t)M * K * 2) || overlaps(y, ybytes, qd, (size_t)K / 2 * N) ||
+        overlaps(y, ybytes, scales, (size_t)G * N * 2) || overlaps(y, ybytes, qzeros, (size_t)G * N / 2))
+        return W4A16_EINVAL;
+    return W4A16_OK;
+}
+
+// Kernel choice per M.  GEMV for M <= 8 when its activation copy fits in
+// shared memory, tensor cores otherwise.
+int choose_path(int M, int N, int K, int sms) {
+    GemvPlan gp;
+    if (M <= 8 && gemv_plan(M, N, K, sms, &gp)) return W4A16_PATH_GEMV;
+    return W4A16_PATH_TC;
+}
+
+size_t ws_for_path(int path, int M, int N, int K, int sms) {
+    if (path == W4A16_PATH_GEMV) {
+        GemvPlan gp;
+        return gemv_plan(M, N, K, sms, &gp) ? gp.ws_bytes : 0;
+    }
+    TcPlan tp;
+    return tc_plan(M, N, K, sms, &tp) ? tp.ws_bytes : 0;
+}
+
+int run_gemm(int path, const void* x, const uint32_t* qd, const void* scales, const uint32_t* qzeros, int M, int N,
+             int K, int group, void* y, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    int st = check_gemm(x, qd, scales, qzeros, M, N, K, group, y);
+    if (st != W4A16_OK) return st;
+    const int dev = current_device();
+    if (dev < 0) return W4A16_ECUDA;
+    const int sms = device_sms(dev);
+    if (sms <= 0) return W4A16_ECUDA;
+    if (path == W4A16_PATH_AUTO) path = choose_path(M, N, K, sms);
+    cudaError_t e;
+    if (path == W4A16_PATH_GEMV) {
+        GemvPlan gp;
+        if (!gemv_plan(M, N, K, sms, &gp)) return W4A16_EUNSUPPORTED;
+        if (gp.ws_bytes && (!ws || ws_bytes < gp.ws_bytes || !aligned16(ws))) return W4A16_EWORKSPACE;
+        e = launch_gemv(static_cast<const uint16_t*>(x), qd, static_cast<const uint16_t*>(scales), qzeros,
+                        static_cast<uint16_t*>(y), M, N, K, ws, gp, stream);
+    } else if (path == W4A16_PATH_TC) {
+        TcPlan tp;
+        if (!tc_plan(M, N, K, sms, &tp)) return W4A16_EUNSUPPORTED;
+        if (tp.ws_bytes && (!ws || ws_bytes < tp.ws_bytes || !aligned16(ws))) return W4A16_EWORKSPACE;
+        e = launch_tc(static_cast<const uint16_t*>(x), qd, static_cast<const uint16_t*>(scales), qzeros,
+                      static_cast<uint16_t*>(y), M, N, K, ws, tp, stream);
+    } else {
+        return W4A16_EINVAL;
+    }
+    if (e != cudaSuccess) return W4A16_ECUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return W4A16_OK;
+}
+
+}  // namespace
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+int w4a16_pack(const uint32_t* qweight, uint32_t* qweight_dev, int K, int N, w4a16_stream_t stream) {
+    if (!qweight || !qweight_dev) return W4A16_EINVAL;
+    int st = check_kn(N, K);
+    if (st != W4A16_OK) return st;
+    if (!aligned16(qweight) || !aligned16(qweight_dev)) return W4A16_EALIGN;
+    const size_t bytes = (size_t)K / 2 * N;
+    if (overlaps(qweight, bytes, qweight_dev, bytes)) return W4A16_EINVAL;
+    if (launch_pack(qweight, qweight_dev, K, N, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return W4A16_ECUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return W4A16_OK;
+}
+
+int w4a16_unpack(const uint32_t* qweight_dev, uint32_t* qweight, int K, int N, w4a16_stream_t stream) {
+    if (!qweight || !qweight_dev) return W4A16_EINVAL;
+    int st = check_kn(N, K);
+    if (st != W4A16_OK) return st;
+    if (!aligned16(qweight) || !aligned16(qweight_dev)) return W4A16_EALIGN;
+    const size_t bytes = (size_t)K / 2 * N;
+    if (overlaps(qweight, bytes, qweight_dev, bytes)) return W4A16_EINVAL;
+    if (launch_unpack(qweight_dev, qweight, K, N, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return W4A16_ECUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return W4A16_OK;
+}
+
+size_t w4a16_workspace_bytes_path(int path, int M, int N, int K, int group) {
+    if (M < 1 || group != 128 || check_kn(N, K) != W4A16_OK) return 0;
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    const int sms = device_sms(dev);
+    if (sms <= 0) return 0;
+    if (path == W4A16_PATH_AUTO) path = choose_path(M, N, K, sms);
+    return ws_for_path(path, M, N, K, sms);
+}
+
+size_t w4a16_workspace_bytes(int M, int N, int K, int group) {
+    return w4a16_workspace_bytes_path(W4A16_PATH_AUTO, M, N, K, group);
+}
+
+size_t w4a16_workspace_bytes_max(int max_M, int N, int K, int group) {
+    size_t best = 0;
+    for (int m = 1; m <= max_M; ++m) {
+        // the plan only changes at token-tile boundaries; probe each M up to 256, then tile edges
+        if (m > 256 && (m % 128) != 0 && m != max_M) continue;
+        for (int path = W4A16_PATH_GEMV; path <= W4A16_PATH_TC; ++path) {
+            size_t b = w4a16_workspace_bytes_path(path, m, N, K, group);
+            if (b > best) best = b;
+        }
+    }
+    return best;
+}
+
+int w4a16_set_workspace(void* workspace, size_t bytes) {
+    const int dev = current_device();
+    if (dev < 0) return W4A16_ECUDA;
+    if (workspace && !aligned16(workspace)) return W4A16_EALIGN;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_ws[dev] = workspace;
+    g_ws_bytes[dev] = workspace ? bytes : 0;
+    return W4A16_OK;
+}
+
+int w4a16_gemm_path(int path, const void* x, const uint32_t* qweight_dev, const void* scales, const uint32_t* qzeros,
+                    int M, int N, int K, int group, void* y, void* workspace, size_t workspace_bytes,
+                    w4a16_stream_t stream) {
+    return run_gemm(path, x, qweight_dev, scales, qzeros, M, N, K, group, y, workspace, workspace_bytes,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int w4a16_gemm_ws(const void* x, const uint32_t* qweight_dev, const void* scales, const uint32_t* qzeros, int M,
+                  int N, int K, int group, void* y, void* workspace, size_t workspace_bytes, w4a16_stream_t stream) {
+    return run_gemm(W4A16_PATH_AUTO, x, qweight_dev, scales, qzeros, M, N, K, group, y, workspace, workspace_bytes,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int w4a16_gemm(const void* x, const uint32_t* qweight_dev, const void* scales, const uint32_t* qzeros, int M, int N,
+               int K, int group, void* y, w4a16_stream_t stream) {
+    const int dev = current_device();
+    if (dev < 0) return W4A16_ECUDA;
+    void* ws;
+    size_t wsb;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        ws = g_ws[dev];
+        wsb = g_ws_bytes[dev];
+    }
+    return run_gemm(W4A16_PATH_AUTO, x, qweight_dev, scales, qzeros, M, N, K, group, y, ws, wsb,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int w4a16_auto_path(int M, int N, int K, int group) {
+    if (M < 1 || group != 128 || check_kn(N, K) != W4A16_OK) return W4A16_EINVAL;
+    const int dev = current_device();
+    if (dev < 0) return W4A16_ECUDA;
+    const int sms = device_sms(dev);
+    if (sms <= 0) return W4A16_ECUDA;
+    return choose_path(M, N, K, sms);
+}
+
+const char* w4a16_status_str(int status) {
+    switch (status) {
+        case W4A16_OK: return "ok";
+        case W4A16_EINVAL: return "invalid argument (null pointer, bad size or overlapping output)";
+        case W4A16_EALIGN: return "pointer not 16-byte aligned";
+        case W4A16_EUNSUPPORTED: return "unsupported problem (group must be 128, K a multiple of 128)";
+        case W4A16_ECUDA: return "CUDA runtime error or failed launch";
+        case W4A16_ETIMEOUT: return "a bounded device-side wait timed out";
+        case W4A16_EWORKSPACE: return "workspace missing, too small or misaligned";
+        default: return "unknown status";
+    }
+}
+
+int w4a16_last_device_status(w4a16_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return W4A16_ECUDA;
+    const int a = gemv_read_status();
+    const int b = tc_read_status();
+    const int c = selftest_read_status();
+    if (a == W4A16_ECUDA || b == W4A16_ECUDA || c == W4A16_ECUDA) return W4A16_ECUDA;
+    if (a != 0) return a;
+    if (b != 0) return b;
+    return c;
+}
+
+int w4a16_selftest_wait_timeout(long long wait_ns, w4a16_stream_t stream) {
+    if (wait_ns < 1000 || wait_ns > 1000000000ll) return W4A16_EINVAL;
+    if (launch_selftest_wait((uint64_t)wait_ns, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return W4A16_ECUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return W4A16_OK;
+}
+
+uint64_t w4a16_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

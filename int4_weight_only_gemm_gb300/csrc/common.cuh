@@ -1,0 +1,308 @@
+// Shared device helpers for the W4A16 kernels (sm_103a).
+//
+// Inline-PTX wrappers for mbarriers, bulk / tensor copies and tcgen05, the
+// bounded waits every pipeline uses, and the device-layout arithmetic that
+// include/w4a16.h defines.  All waits are bounded: on expiry they record
+// W4A16_ETIMEOUT in the translation unit's status word and return false, so a
+// lost arrival ends the kernel with an error status instead of a hang.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "w4a16.h"
+
+#define W4A16_DEVICE __device__ __forceinline__
+
+namespace w4a16 {
+
+// ---------------------------------------------------------------------------
+// device layout of the packed weights (see the header for the definition)
+// ---------------------------------------------------------------------------
+struct Layout {
+    int K, N, KB, NB;  // KB = K/128 blocks, NB = ceil(N/128) column tiles
+    __host__ __device__ Layout(int K_, int N_) : K(K_), N(N_), KB(K_ / 128), NB((N_ + 127) / 128) {}
+    __host__ __device__ int width(int nb) const { return N - 128 * nb < 128 ? N - 128 * nb : 128; }
+    // word offset of block (nb, kb)
+    __host__ __device__ size_t block_word(int nb, int kb) const {
+        return (size_t)128 * 16 * KB * nb + (size_t)kb * width(nb) * 16;
+    }
+};
+
+// position of nibble for row offset r (0..7) inside a device word
+__host__ __device__ inline int dev_nibble_pos(int r) { return (r & 1) ? 4 + (r >> 1) : (r >> 1); }
+
+// ---------------------------------------------------------------------------
+// time and status
+// ---------------------------------------------------------------------------
+// Wall-clock bound of any single wait (nanoseconds) and a spin cap.
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint32_t kWaitSpins = 1u << 26;
+
+W4A16_DEVICE uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+W4A16_DEVICE uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+W4A16_DEVICE uint32_t lane_id() {
+    uint32_t l;
+    asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
+    return l;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+W4A16_DEVICE void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+W4A16_DEVICE void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+W4A16_DEVICE void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+W4A16_DEVICE void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+W4A16_DEVICE void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+W4A16_DEVICE bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.  `abort` is a
+// shared flag: once any thread of the CTA has given up, the others stop
+// waiting at once.  Returns false on timeout or abort.
+W4A16_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                            uint64_t limit_ns = kWaitNs) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 0; i < kWaitSpins; ++i) {
+        if (mbar_try_wait(a, parity)) return true;
+        if ((i & 63) == 63) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > limit_ns) {
+                *abort = 1;
+                atomicExch(status, (int)W4A16_ETIMEOUT);
+                return false;
+            }
+        }
+    }
+    *abort = 1;
+    atomicExch(status, (int)W4A16_ETIMEOUT);
+    return false;
+}
+
+// Warp-uniform bounded wait: lane 0 polls, every lane gets the same answer, so
+// the warp-collective tcgen05 instructions that follow never diverge.
+W4A16_DEVICE bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+    int ok = 0;
+    if (lane_id() == 0) ok = mbar_wait(bar, parity, abort, status) ? 1 : 0;
+    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+// AND of `pred` over the `count` threads of named barrier `id` (all must arrive).
+W4A16_DEVICE bool bar_and(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// ---------------------------------------------------------------------------
+// bulk and tensor copies (TMA), global -> shared, completion on an mbarrier
+// ---------------------------------------------------------------------------
+W4A16_DEVICE void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+W4A16_DEVICE void tma_load_2d(void* smem_dst, const void* tmap, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+W4A16_DEVICE void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (tensor memory and 5th-generation MMA)
+// ---------------------------------------------------------------------------
+W4A16_DEVICE void tmem_alloc(uint32_t* smem_result, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_result)),
+                 "r"(ncols)
+                 : "memory");
+}
+W4A16_DEVICE void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+W4A16_DEVICE void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+W4A16_DEVICE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+W4A16_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16 (bf16 inputs, f32 accumulate)
+W4A16_DEVICE void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// arrive on the mbarrier once all earlier tcgen05 async ops of this thread are done
+W4A16_DEVICE void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// 32 lanes x 32 bits, 8 consecutive columns per thread
+W4A16_DEVICE void tmem_st_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(v[0]),
+        "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+        : "memory");
+}
+W4A16_DEVICE void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+W4A16_DEVICE void tmem_ld_x16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+W4A16_DEVICE void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart.  `addr` must keep the 1024-byte
+// alignment of the swizzle atom except for the K offset inside the row.
+W4A16_DEVICE uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFF) >> 4);          // start address
+    d |= (uint64_t)(16 >> 4) << 16;                  // leading byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset: next 8 rows
+    d |= (uint64_t)1 << 46;                          // descriptor version
+    d |= (uint64_t)2 << 61;                          // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, f32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// numeric helpers
+// ---------------------------------------------------------------------------
+// bfloat16 pair (128 + code_lo, 128 + code_hi) from the nibbles at bit 4p and
+// bit 4p + 16 of a device word: an exact integer-to-bfloat16 conversion.
+W4A16_DEVICE uint32_t magic_pair(uint32_t w, int p) {
+    uint32_t r;
+    const uint32_t s = w >> (4 * p);
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(s), "r"(0x000F000Fu), "r"(0x43004300u));
+    return r;  // (s & 0x000F000F) | 0x43004300
+}
+
+W4A16_DEVICE float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+W4A16_DEVICE float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// d = a.lo * b.lo + c  /  a.hi * b.hi + c  with bf16 inputs, f32 accumulate
+W4A16_DEVICE float fma_lo(uint32_t a, uint32_t b, float c) {
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+W4A16_DEVICE float fma_hi(uint32_t a, uint32_t b, float c) {
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+
+W4A16_DEVICE uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+W4A16_DEVICE uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+W4A16_DEVICE uint16_t f32_to_bf16_rn(float f) {
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+    return r;
+}
+
+W4A16_DEVICE float f16_bits_to_f32(uint16_t h) {
+    float f;
+    asm("{\n\t.reg .f16 t;\n\tmov.b16 t, %1;\n\tcvt.f32.f16 %0, t;\n\t}" : "=f"(f) : "h"(h));
+    return f;
+}
+
+// ---------------------------------------------------------------------------
+// split-K fix-up: ordered reduction of partial tiles by the last arrival
+// ---------------------------------------------------------------------------
+// Workspace layout shared by the kernels: a fixed 64 KB area of per-tile
+// arrival counters (uint32), then the partial sums (float).  The counter area
+// has the same place and size for every problem, so partial sums of one call
+// never land where another call keeps its counters; each counter returns to
+// zero after its tile's last contributor reduced it.
+constexpr size_t kCounterBytes = 64 * 1024;
+constexpr size_t kMaxCounters = kCounterBytes / 4;
+__host__ __device__ inline size_t ws_counter_bytes(size_t) { return kCounterBytes; }
+
+}  // namespace w4a16

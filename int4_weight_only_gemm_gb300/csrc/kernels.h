@@ -1,0 +1,38 @@
+// Internal interface between the C ABI layer and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace w4a16 {
+
+cudaError_t launch_pack(const uint32_t* q, uint32_t* qd, int K, int N, cudaStream_t s);
+cudaError_t launch_unpack(const uint32_t* qd, uint32_t* q, int K, int N, cudaStream_t s);
+
+// CUDA-core split-K GEMV (M <= 8)
+struct GemvPlan {
+    int ctas, P;     // CTAs, workers (warpgroups)
+    long long C;     // 2 KB chunks
+    size_t smem, ws_bytes;
+};
+bool gemv_plan(int M, int N, int K, int sms, GemvPlan* out);
+cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
+                        uint16_t* y, int M, int N, int K, void* ws, const GemvPlan& plan, cudaStream_t s);
+int gemv_read_status();
+
+// tcgen05 tensor-core GEMM (any M)
+struct TcPlan {
+    int NT, MT, NB, splits;  // tokens per tile, token tiles, column tiles, K splits
+    size_t smem, ws_bytes;
+};
+bool tc_plan(int M, int N, int K, int sms, TcPlan* out);
+cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
+                      uint16_t* y, int M, int N, int K, void* ws, const TcPlan& plan, cudaStream_t s);
+int tc_read_status();
+
+// failure-detection self-test
+cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t s);
+int selftest_read_status();
+
+}  // namespace w4a16

@@ -1,0 +1,261 @@
+"""GPU parity of the W4A16 GEMM (through the C ABI) against the CPU oracle.
+
+Workloads are the seeded synthetic problems of w4a16_inputs: the tiny case,
+the decode set (M=1) and verify set (M=16) over the four projection shapes of
+a ~4B decoder layer, prefill (M=2048), the M sweep up to 8192 and the
+vocabulary-shaped GEMM ("Quantize the Target, Quantize the Drafter":
+pith.science review -- INT4 target and drafter, group size 128, DFlash block
+size 16).  Small problems are compared in full; full-size ones on sampled
+outputs computed one by one by the oracle.  Both kernels (GEMV and tensor
+core) are checked at every M either can run.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w4a16_inputs as wi
+from tests.gpu_helpers import Device, bf16_bits, bf16_to_f64, check_close, check_sampled
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+GEMV, TC, AUTO = 1, 2, 0
+
+
+def _full(prob, y, what):
+    ref = oracle.gemm(prob.x, prob.qweight, prob.scales, prob.qzeros)
+    return check_close(bf16_to_f64(y), ref, what)
+
+
+# ---- config 0: tiny -----------------------------------------------------------
+
+@pytest.mark.parametrize("path", [AUTO, GEMV, TC])
+def test_tiny_config(path):
+    p = wi.generate_named("tiny", 1, 0)
+    d = Device(p)
+    y = d.run(path)
+    _full(p, y, f"tiny path={path}")
+    # stored values written by tests/golden/make_golden.py from the oracle
+    vals = [float.fromhex(l) for l in open(os.path.join(GOLDEN, "tiny_m1_k256_n128.txt"))
+            if l.strip() and not l.startswith("#")]
+    check_close(bf16_to_f64(y)[0], np.array(vals), "tiny vs golden")
+
+
+# ---- config 1 / 2: decode (M=1) and verify (M=16) sets, in full ---------------
+
+@pytest.mark.parametrize("shape", wi.LAYER)
+@pytest.mark.parametrize("path", [AUTO, GEMV, TC])
+def test_decode_set_m1(shape, path):
+    p = wi.generate_named(shape, 1, 1)
+    y = Device(p).run(path)
+    _full(p, y, f"decode {shape} path={path}")
+
+
+@pytest.mark.parametrize("shape", wi.LAYER)
+def test_verify_set_m16(shape):
+    p = wi.generate_named(shape, 16, 2)
+    y = Device(p).run(AUTO)
+    _full(p, y, f"verify {shape}")
+
+
+# ---- config 3: prefill M=2048, sampled ----------------------------------------
+
+@pytest.mark.parametrize("shape", wi.LAYER)
+def test_prefill_m2048_sampled(shape):
+    p = wi.generate_named(shape, 2048, 3)
+    d = Device(p)
+    y = d.run(AUTO)
+    check_sampled(d, y, 4000, seed=3, what=f"prefill {shape}")
+    # two whole rows in full, first and last token
+    rows = np.array([0, 2047])
+    ref = oracle.gemm(p.x[rows], p.qweight, p.scales, p.qzeros)
+    check_close(bf16_to_f64(y[torch.as_tensor(rows, device=y.device)]), ref, f"prefill {shape} rows")
+
+
+# ---- config 4: M sweep and the vocabulary shape ------------------------------
+
+@pytest.mark.parametrize("M", [2, 4, 8])
+@pytest.mark.parametrize("shape", wi.LAYER)
+def test_sweep_small_m_both_paths(M, shape):
+    p = wi.generate_named(shape, M, 4)
+    d = Device(p)
+    ref = oracle.gemm(p.x, p.qweight, p.scales, p.qzeros)
+    for path in (GEMV, TC):
+        check_close(bf16_to_f64(d.run(path)), ref, f"sweep {shape} M={M} path={path}")
+
+
+@pytest.mark.parametrize("M", [16, 32])
+@pytest.mark.parametrize("shape", wi.LAYER)
+def test_sweep_mid_m_full(M, shape):
+    p = wi.generate_named(shape, M, 4)
+    _full(p, Device(p).run(AUTO), f"sweep {shape} M={M}")
+
+
+@pytest.mark.parametrize("M", [64, 128, 8192])
+@pytest.mark.parametrize("shape", wi.LAYER)
+def test_sweep_large_m_sampled(M, shape):
+    p = wi.generate_named(shape, M, 4)
+    d = Device(p)
+    check_sampled(d, d.run(AUTO), 3000, seed=M, what=f"sweep {shape} M={M}")
+
+
+@pytest.mark.parametrize("M,path", [(1, GEMV), (1, TC), (16, TC)])
+def test_vocab_shape(M, path):
+    p = wi.generate_named("vocab", M, 4)
+    d = Device(p)
+    y = d.run(path)
+    check_sampled(d, y, 6000, seed=5, what=f"vocab M={M} path={path}")
+    rows = np.array([0, M - 1])
+    ref = oracle.gemm(p.x[rows], p.qweight, p.scales, p.qzeros)
+    check_close(bf16_to_f64(y[torch.as_tensor(rows, device=y.device)]), ref, f"vocab M={M} rows")
+
+
+# ---- edge cases: ragged tiles, odd M, one group --------------------------------
+
+EDGE = [(M, K, N) for (K, N) in [(128, 8), (128, 136), (384, 264), (1024, 392)]
+        for M in (1, 3, 7, 13, 17, 31, 33, 100, 129)]
+
+
+@pytest.mark.parametrize("M,K,N", EDGE)
+def test_ragged_and_odd_shapes(M, K, N):
+    p = wi.generate(M, K, N, seed=M * 7 + K + N)
+    d = Device(p)
+    ref = oracle.gemm(p.x, p.qweight, p.scales, p.qzeros)
+    paths = [GEMV, TC] if M <= 8 else [TC]
+    for path in paths:
+        check_close(bf16_to_f64(d.run(path)), ref, f"M={M} K={K} N={N} path={path}")
+
+
+@pytest.mark.parametrize("M", [1, 5, 16, 40])
+def test_exact_case_bit_exact(M):
+    """x in {-1, 0, 1} with at most 8 nonzeros per row and s = 2^-6: every
+    partial sum is exact in f32 and y*64 is an integer of magnitude <= 120, so
+    y is exact in bfloat16 and every correct accumulation order gives the
+    same bits as the oracle's exact value."""
+    r = np.random.default_rng(100 + M)
+    K, N = 256, 264
+    xv = np.zeros((M, K))
+    for m in range(M):
+        nz = r.choice(K, size=8, replace=False)
+        xv[m, nz] = r.choice([-1.0, 1.0], size=8)
+    x = (xv.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    qw = r.integers(0, 1 << 32, size=(K // 8, N), dtype=np.uint64).astype(np.uint32)
+    qz = r.integers(0, 1 << 32, size=(K // 128, N // 8), dtype=np.uint64).astype(np.uint32)
+    s = np.full((K // 128, N), 2.0 ** -6, dtype=np.float16).view(np.uint16)
+    p = wi.Problem(M, K, N, 128, x, qw, s, qz)
+    ref = oracle.gemm(x, qw, s, qz)
+    want = oracle.f64_to_bf16(ref)
+    assert np.array_equal(oracle.bf16_to_f64(want), ref)  # exact in bf16
+    d = Device(p)
+    for path in ([GEMV, TC] if M <= 8 else [TC]):
+        got = bf16_bits(d.run(path))
+        assert np.array_equal(got, want), f"path {path}: {np.count_nonzero(got != want)} bits differ"
+
+
+def test_zero_codes_give_zero():
+    K, N, M = 512, 256, 4
+    r = np.random.default_rng(1)
+    x = wi.f32_to_bf16_bits(r.standard_normal((M, K)).astype(np.float32))
+    qw = np.zeros((K // 8, N), np.uint32)
+    qz = np.zeros((K // 128, N // 8), np.uint32)
+    s = wi.f64_to_f16_bits(r.uniform(0.001, 0.02, (K // 128, N)))
+    d = Device(wi.Problem(M, K, N, 128, x, qw, s, qz))
+    for path in (GEMV, TC):
+        y = d.run(path)
+        assert torch.count_nonzero(y.float()).item() == 0
+
+
+# ---- determinism, workspace reuse, streams ------------------------------------
+
+@pytest.mark.parametrize("shape,M,path", [("o_proj", 1, GEMV), ("down", 4, GEMV), ("o_proj", 16, TC),
+                                          ("down", 16, TC), ("qkv", 2048, TC)])
+def test_deterministic_and_workspace_reused(shape, M, path):
+    p = wi.generate_named(shape, M, 9)
+    d = Device(p)
+    import int4_weight_only_gemm_gb300 as w
+    ws = w.new_workspace(w.w4a16_workspace_bytes(M, p.N, p.K, path=path))
+    y1 = d.run(path, workspace=ws)
+    y2 = d.run(path, workspace=ws)
+    y3 = d.run(path, workspace=ws)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y3.view(torch.int16))
+    # counters are back at zero after every call
+    nz = ws.view(torch.int32)[:16384].abs().sum().item() if ws.numel() >= 65536 else 0
+    assert nz == 0
+    check_sampled(d, y3, 1500, seed=1, what=f"{shape} M={M} reuse")
+
+
+def test_registered_workspace_and_default_signature():
+    import ctypes
+    import int4_weight_only_gemm_gb300 as w
+    p = wi.generate_named("qkv", 1, 11)
+    d = Device(p)
+    lib = w.load_library()
+    need = w.w4a16_workspace_bytes(1, p.N, p.K)
+    y = torch.empty((1, p.N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    if need:
+        w.w4a16_set_workspace(None)
+        st = lib.w4a16_gemm(d.x.data_ptr(), d.qd.data_ptr(), d.scales.data_ptr(), d.qzeros.data_ptr(),
+                            1, p.N, p.K, 128, y.data_ptr(), stream)
+        assert st == w.W4A16_EWORKSPACE
+    ws = w.new_workspace(need)
+    w.w4a16_set_workspace(ws)
+    try:
+        st = lib.w4a16_gemm(d.x.data_ptr(), d.qd.data_ptr(), d.scales.data_ptr(), d.qzeros.data_ptr(),
+                            1, p.N, p.K, 128, y.data_ptr(), stream)
+        assert st == 0
+        torch.cuda.synchronize()
+        _full(p, y, "registered workspace")
+        assert w.w4a16_last_device_status() == 0
+    finally:
+        w.w4a16_set_workspace(None)
+    # too small an explicit workspace is refused before launch
+    if need:
+        small = w.new_workspace(need // 2)
+        st = w.w4a16_gemm_raw(d.x.data_ptr(), d.qd.data_ptr(), d.scales.data_ptr(), d.qzeros.data_ptr(),
+                              1, p.N, p.K, 128, y.data_ptr(), small.data_ptr(), need // 2)
+        assert st == w.W4A16_EWORKSPACE
+
+
+def test_side_stream():
+    p = wi.generate_named("o_proj", 16, 12)
+    d = Device(p)
+    import int4_weight_only_gemm_gb300 as w
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        y = w.w4a16_gemm(d.x, d.qd, d.scales, d.qzeros, stream=s)
+    s.synchronize()
+    _full(p, y, "side stream")
+
+
+def test_gpu_argument_errors():
+    import int4_weight_only_gemm_gb300 as w
+    p = wi.generate_named("tiny", 1, 0)
+    d = Device(p)
+    with pytest.raises(w.W4A16Error) as e:
+        w.w4a16_gemm(d.x, d.qd, d.scales[:1].contiguous(), d.qzeros[:1].contiguous(), group=256)
+    assert e.value.status == w.W4A16_EUNSUPPORTED
+    with pytest.raises(w.W4A16Error) as e:
+        w.w4a16_gemm(d.x.repeat(9, 1), d.qd, d.scales, d.qzeros, path=GEMV)  # M=9 beyond the GEMV
+    assert e.value.status == w.W4A16_EUNSUPPORTED
+    assert w.w4a16_last_device_status() == 0
+
+
+def test_one_workspace_across_shapes_and_paths():
+    """A single workspace serves any sequence of calls: split-K partial sums
+    of one problem must never disturb the arrival counters of the next."""
+    import int4_weight_only_gemm_gb300 as w
+    seq = [("down", 16, TC), ("gate_up", 1, GEMV), ("o_proj", 1, GEMV), ("vocab", 1, GEMV),
+           ("qkv", 16, TC), ("gate_up", 4, GEMV)]
+    need = max(w.w4a16_workspace_bytes(M, *reversed(wi.shape_kn(s)), path=pth) for s, M, pth in seq)
+    ws = w.new_workspace(need)
+    for i, (shape, M, path) in enumerate(seq):
+        p = wi.generate_named(shape, M, 20 + i)
+        d = Device(p)
+        y = d.run(path, workspace=ws)
+        check_sampled(d, y, 2000, seed=i, what=f"shared workspace {shape} M={M}")
