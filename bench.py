@@ -225,7 +225,7 @@ class Workload:
         self.bytes = sum(gemm_bytes(g["M"], g["K"], g["N"]) for g in self.gemms)
         self.flops = sum(gemm_flops(g["M"], g["K"], g["N"]) for g in self.gemms)
 
-    def launch_step(self, copy, stream_ptr, only=None):
+    def launch_step(self, copy, stream_ptr, only=None, flags=None):
         w = self.w
         n = 0
         for i, g in enumerate(self.gemms):
@@ -233,32 +233,32 @@ class Workload:
                 continue
             st = w.w4a16_gemm_raw(g["x"].data_ptr(), g["qds"][copy].data_ptr(), g["sc"].data_ptr(),
                                   g["qz"].data_ptr(), g["M"], g["N"], g["K"], 128, g["y"].data_ptr(),
-                                  g["ws"].data_ptr(), g["ws_bytes"], 0, stream_ptr)
+                                  g["ws"].data_ptr(), g["ws_bytes"], 0, stream_ptr, flags)
             if st != 0:
                 raise RuntimeError(f"w4a16_gemm failed: {w.w4a16_status_str(st)}")
             n += 1
         return n
 
-    def graphs(self, only=None):
+    def graphs(self, only=None, flags=None):
         """One graph per weight copy (a step each) and one for the whole rotation."""
         torch = self.torch
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
             for c in range(self.copies):  # warm-up outside capture
-                self.launch_step(c, s.cuda_stream, only)
+                self.launch_step(c, s.cuda_stream, only, flags)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         per_step = []
         for c in range(self.copies):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                self.launch_step(c, torch.cuda.current_stream().cuda_stream, only)
+                self.launch_step(c, torch.cuda.current_stream().cuda_stream, only, flags)
             per_step.append(g)
         rot = torch.cuda.CUDAGraph()
         with torch.cuda.graph(rot):
             for c in range(self.copies):
-                self.launch_step(c, torch.cuda.current_stream().cuda_stream, only)
+                self.launch_step(c, torch.cuda.current_stream().cuda_stream, only, flags)
         torch.cuda.synchronize()
         return per_step, rot
 
@@ -407,6 +407,14 @@ def main():
             per[g["shape"]] = {"us": t_ms / n * 1e3, "GB/s": b * n / (t_ms / 1e3) / 1e9,
                                "frac": b * n / (t_ms / 1e3) / 1e9 / hbm}
         extra["decode_m1_per_gemm"] = per
+        # the decode set under each launch-flag combination
+        fl = {}
+        for flags, name in ((0, "plain"), (1, "pdl"), (3, "pdl_static_weights")):
+            ps, rt = wl.graphs(flags=flags)
+            n = max(200, min(args.steps, 20000))
+            t_ms = time_graph_steps(torch, ps, rt, COPIES, n, 50)
+            fl[name] = {"us_per_step": t_ms / n * 1e3, "GB/s": wl.bytes * n / (t_ms / 1e3) / 1e9}
+        extra["decode_m1_flags"] = fl
         for cfg, unit in ((2, "GB/s"), (3, "TFLOP/s")):
             name, seed, items = wi.CONFIGS[cfg]
             copies = COPIES if cfg == 2 else 2
@@ -420,8 +428,16 @@ def main():
             else:
                 v = wl2.flops * n / (t_ms / 1e3) / 1e12
                 frac = v / bf16_peak
+            per2 = {}
+            for i, g in enumerate(wl2.gemms):
+                ps1, rt1 = wl2.graphs(only=i)
+                n1 = 2000 if cfg == 2 else 20
+                t1 = time_graph_steps(torch, ps1, rt1, copies, n1, 5)
+                per2[g["shape"]] = {"us": t1 / n1 * 1e3,
+                                    "GB/s": gemm_bytes(g["M"], g["K"], g["N"]) * n1 / (t1 / 1e3) / 1e9,
+                                    "TFLOP/s": gemm_flops(g["M"], g["K"], g["N"]) * n1 / (t1 / 1e3) / 1e12}
             extra[name] = {"value": v, "unit": unit, "frac": frac, "ms_per_step": t_ms / n,
-                           "workload": ", ".join(f"{s} M={M}" for s, M in items)}
+                           "workload": ", ".join(f"{s} M={M}" for s, M in items), "per_gemm": per2}
             del wl2, ps, rt
             torch.cuda.empty_cache()
 

@@ -135,6 +135,25 @@ int w4a16_gemm_path(int path, const void *x, const uint32_t *qweight_dev,
                     int group, void *y, void *workspace, size_t workspace_bytes,
                     w4a16_stream_t stream);
 
+/* Launch flags for w4a16_gemm_ex. */
+enum {
+    /* Launch as a programmatic dependent of the preceding work in the stream:
+     * the kernel may be scheduled while that work finishes, but reads x, y,
+     * the workspace (and, without the next flag, the weights) only after it
+     * has completed.  The entry points without a flags argument set it. */
+    W4A16_FLAG_PDL = 1u << 0,
+    /* With W4A16_FLAG_PDL: the packed weights, scales and zeros are not
+     * written by work still in flight on the stream (true for a model whose
+     * weights were packed earlier), so the kernel may start streaming them
+     * before the preceding work completes. */
+    W4A16_FLAG_STATIC_WEIGHTS = 1u << 1
+};
+
+/* As w4a16_gemm_path with explicit launch flags (W4A16_EINVAL for unknown bits). */
+int w4a16_gemm_ex(int path, unsigned flags, const void *x, const uint32_t *qweight_dev,
+                  const void *scales, const uint32_t *qzeros, int M, int N, int K, int group,
+                  void *y, void *workspace, size_t workspace_bytes, w4a16_stream_t stream);
+
 /* Workspace bytes for a given path (0 if none); 0 for unsupported input. */
 size_t w4a16_workspace_bytes_path(int path, int M, int N, int K, int group);
 

@@ -34,6 +34,7 @@ W4A16_ECUDA = -4
 W4A16_ETIMEOUT = -5
 W4A16_EWORKSPACE = -6
 PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
+FLAG_PDL, FLAG_STATIC_WEIGHTS = 1, 2
 
 _lib = None
 _lock = threading.Lock()
@@ -67,6 +68,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.w4a16_gemm.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, vp, vp]
             lib.w4a16_gemm_ws.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, vp, vp, sz, vp]
             lib.w4a16_gemm_path.argtypes = [ci, vp, vp, vp, vp, ci, ci, ci, ci, vp, vp, sz, vp]
+            lib.w4a16_gemm_ex.argtypes = [ci, ctypes.c_uint, vp, vp, vp, vp, ci, ci, ci, ci, vp, vp, sz, vp]
             lib.w4a16_auto_path.argtypes = [ci, ci, ci, ci]
             lib.w4a16_status_str.argtypes = [ci]
             lib.w4a16_status_str.restype = ctypes.c_char_p
@@ -161,8 +163,11 @@ def _cached_workspace(nbytes: int, device: torch.device) -> torch.Tensor:
 
 def w4a16_gemm(x: torch.Tensor, qweight_dev: torch.Tensor, scales: torch.Tensor, qzeros: torch.Tensor,
                group: int = 128, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-               path: int = PATH_AUTO, stream=None) -> torch.Tensor:
-    """y = x . dequant(qweight_dev, scales, qzeros) in bf16, on the GPU kernels."""
+               path: int = PATH_AUTO, stream=None, flags: int | None = None) -> torch.Tensor:
+    """y = x . dequant(qweight_dev, scales, qzeros) in bf16, on the GPU kernels.
+
+    flags=None uses the library's default launch flags; otherwise a mask of
+    FLAG_PDL and FLAG_STATIC_WEIGHTS (see include/w4a16.h)."""
     _check(x, "x", torch.bfloat16)
     if x.dim() != 2:
         raise ValueError("x must be [M, K]")
@@ -181,18 +186,26 @@ def w4a16_gemm(x: torch.Tensor, qweight_dev: torch.Tensor, scales: torch.Tensor,
         workspace = _cached_workspace(need, x.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = lib.w4a16_gemm_path(path, x.data_ptr(), qweight_dev.data_ptr(), scales.data_ptr(), qzeros.data_ptr(),
-                             M, N, K, group, out.data_ptr(), ws_ptr, ws_bytes, _stream(stream))
+    if flags is None:
+        st = lib.w4a16_gemm_path(path, x.data_ptr(), qweight_dev.data_ptr(), scales.data_ptr(), qzeros.data_ptr(),
+                                 M, N, K, group, out.data_ptr(), ws_ptr, ws_bytes, _stream(stream))
+    else:
+        st = lib.w4a16_gemm_ex(path, flags, x.data_ptr(), qweight_dev.data_ptr(), scales.data_ptr(),
+                               qzeros.data_ptr(), M, N, K, group, out.data_ptr(), ws_ptr, ws_bytes, _stream(stream))
     _raise(st, "w4a16_gemm")
     return out
 
 
 def w4a16_gemm_raw(x_ptr: int, qd_ptr: int, scales_ptr: int, qzeros_ptr: int, M: int, N: int, K: int,
                    group: int, y_ptr: int, ws_ptr: int | None, ws_bytes: int, path: int = PATH_AUTO,
-                   stream: int = 0) -> int:
+                   stream: int = 0, flags: int | None = None) -> int:
     """Pointer-level call (no checks beyond the library's own), for timing loops."""
-    return load_library().w4a16_gemm_path(path, x_ptr, qd_ptr, scales_ptr, qzeros_ptr, M, N, K, group, y_ptr,
-                                          ws_ptr, ws_bytes, stream)
+    lib = load_library()
+    if flags is None:
+        return lib.w4a16_gemm_path(path, x_ptr, qd_ptr, scales_ptr, qzeros_ptr, M, N, K, group, y_ptr,
+                                   ws_ptr, ws_bytes, stream)
+    return lib.w4a16_gemm_ex(path, flags, x_ptr, qd_ptr, scales_ptr, qzeros_ptr, M, N, K, group, y_ptr,
+                             ws_ptr, ws_bytes, stream)
 
 
 def w4a16_auto_path(M: int, N: int, K: int, group: int = 128) -> int:

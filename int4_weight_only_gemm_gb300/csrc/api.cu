@@ -85,8 +85,15 @@ size_t ws_for_path(int path, int M, int N, int K, int sms) {
     return tc_plan(M, N, K, sms, &tp) ? tp.ws_bytes : 0;
 }
 
-int run_gemm(int path, const void* x, const uint32_t* qd, const void* scales, const uint32_t* qzeros, int M, int N,
-             int K, int group, void* y, void* ws, size_t ws_bytes, cudaStream_t stream) {
+// Launch flags used by the entry points that take none: programmatic dependent
+// launch, which changes no ordering (every kernel waits for the preceding grid
+// before it touches global memory) but lets its launch overlap that grid's end.
+constexpr unsigned kDefaultFlags = W4A16_FLAG_PDL;
+constexpr unsigned kKnownFlags = W4A16_FLAG_PDL | W4A16_FLAG_STATIC_WEIGHTS;
+
+int run_gemm(int path, unsigned flags, const void* x, const uint32_t* qd, const void* scales, const uint32_t* qzeros,
+             int M, int N, int K, int group, void* y, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (flags & ~kKnownFlags) return W4A16_EINVAL;
     int st = check_gemm(x, qd, scales, qzeros, M, N, K, group, y);
     if (st != W4A16_OK) return st;
     const int dev = current_device();
@@ -100,13 +107,13 @@ int run_gemm(int path, const void* x, const uint32_t* qd, const void* scales, co
         if (!gemv_plan(M, N, K, sms, &gp)) return W4A16_EUNSUPPORTED;
         if (gp.ws_bytes && (!ws || ws_bytes < gp.ws_bytes || !aligned16(ws))) return W4A16_EWORKSPACE;
         e = launch_gemv(static_cast<const uint16_t*>(x), qd, static_cast<const uint16_t*>(scales), qzeros,
-                        static_cast<uint16_t*>(y), M, N, K, ws, gp, stream);
+                        static_cast<uint16_t*>(y), M, N, K, ws, gp, stream, flags);
     } else if (path == W4A16_PATH_TC) {
         TcPlan tp;
         if (!tc_plan(M, N, K, sms, &tp)) return W4A16_EUNSUPPORTED;
         if (tp.ws_bytes && (!ws || ws_bytes < tp.ws_bytes || !aligned16(ws))) return W4A16_EWORKSPACE;
         e = launch_tc(static_cast<const uint16_t*>(x), qd, static_cast<const uint16_t*>(scales), qzeros,
-                      static_cast<uint16_t*>(y), M, N, K, ws, tp, stream);
+                      static_cast<uint16_t*>(y), M, N, K, ws, tp, stream, flags);
     } else {
         return W4A16_EINVAL;
     }
@@ -188,14 +195,21 @@ int w4a16_set_workspace(void* workspace, size_t bytes) {
 int w4a16_gemm_path(int path, const void* x, const uint32_t* qweight_dev, const void* scales, const uint32_t* qzeros,
                     int M, int N, int K, int group, void* y, void* workspace, size_t workspace_bytes,
                     w4a16_stream_t stream) {
-    return run_gemm(path, x, qweight_dev, scales, qzeros, M, N, K, group, y, workspace, workspace_bytes,
+    return run_gemm(path, kDefaultFlags, x, qweight_dev, scales, qzeros, M, N, K, group, y, workspace,
+                    workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int w4a16_gemm_ex(int path, unsigned flags, const void* x, const uint32_t* qweight_dev, const void* scales,
+                  const uint32_t* qzeros, int M, int N, int K, int group, void* y, void* workspace,
+                  size_t workspace_bytes, w4a16_stream_t stream) {
+    return run_gemm(path, flags, x, qweight_dev, scales, qzeros, M, N, K, group, y, workspace, workspace_bytes,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 int w4a16_gemm_ws(const void* x, const uint32_t* qweight_dev, const void* scales, const uint32_t* qzeros, int M,
                   int N, int K, int group, void* y, void* workspace, size_t workspace_bytes, w4a16_stream_t stream) {
-    return run_gemm(W4A16_PATH_AUTO, x, qweight_dev, scales, qzeros, M, N, K, group, y, workspace, workspace_bytes,
-                    reinterpret_cast<cudaStream_t>(stream));
+    return run_gemm(W4A16_PATH_AUTO, kDefaultFlags, x, qweight_dev, scales, qzeros, M, N, K, group, y, workspace,
+                    workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int w4a16_gemm(const void* x, const uint32_t* qweight_dev, const void* scales, const uint32_t* qzeros, int M, int N,
@@ -209,7 +223,7 @@ int w4a16_gemm(const void* x, const uint32_t* qweight_dev, const void* scales, c
         ws = g_ws[dev];
         wsb = g_ws_bytes[dev];
     }
-    return run_gemm(W4A16_PATH_AUTO, x, qweight_dev, scales, qzeros, M, N, K, group, y, ws, wsb,
+    return run_gemm(W4A16_PATH_AUTO, kDefaultFlags, x, qweight_dev, scales, qzeros, M, N, K, group, y, ws, wsb,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 

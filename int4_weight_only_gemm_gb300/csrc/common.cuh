@@ -56,6 +56,16 @@ W4A16_DEVICE uint32_t lane_id() {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Wait until the grids this one depends on (the preceding work in the stream,
+// when launched as a programmatic dependent) have completed and their memory
+// is visible.  Returns at once for an ordinary launch.
+W4A16_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next programmatic-dependent grid in the stream be scheduled.
+W4A16_DEVICE void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 W4A16_DEVICE void mbar_init(uint64_t* bar, uint32_t count) {

@@ -50,6 +50,7 @@ struct TcParams {
     int M, N, K, G;
     int NB, MT;      // column tiles, token tiles
     int splits;      // K splits (groups divided evenly)
+    int prefetch;    // weights may be loaded before the preceding grid completes
 };
 
 template <int NT>
@@ -118,24 +119,40 @@ __global__ void __launch_bounds__(kThreads, NT <= 32 ? 2 : 1) tc_gemm_kernel(con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // everything but the producer thread reads global memory only after the
+    // preceding grid has completed (the producer waits in its own loop)
+    if (!(warp == 0 && lane == 0)) pdl_wait();
 
     if (warp == 0) {
         // ---------------- producer ----------------
         if (lane == 0) {
             int issued = 0;
+            const uint32_t pbytes = (uint32_t)W * 32;  // W columns x 8 words
+            // with static weights, the first ring's weight slabs go out before
+            // waiting on the preceding grid; x only after it
+            const int pre = p.prefetch ? (n_stages < kStages ? n_stages : kStages) : 0;
+            for (int it = 0; it < pre; ++it) {
+                const int kb = g_begin + (it >> 1);
+                mbar_arrive_expect_tx(&full[it], pbytes + S::kXStage);
+                bulk_g2s(smem + S::kPOff + it * kPackedStageBytes,
+                         p.qd + L.block_word(nb, kb) + (size_t)(it & 1) * 2 * W * 4, pbytes, &full[it]);
+            }
+            pdl_wait();
             for (int it = 0; it < n_stages; ++it) {
                 const int s = it % kStages;
                 const int use = it / kStages;
-                if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, abort_flag, &g_tc_status)) break;
                 const int kb = g_begin + (it >> 1);
                 const int half = it & 1;
-                const uint32_t pbytes = (uint32_t)W * 32;  // W columns x 8 words
-                mbar_arrive_expect_tx(&full[s], pbytes + S::kXStage);
-                const uint32_t* src = p.qd + L.block_word(nb, kb) + (size_t)half * 2 * W * 4;
-                bulk_g2s(smem + S::kPOff + s * kPackedStageBytes, src, pbytes, &full[s]);
+                if (it >= pre) {
+                    if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, abort_flag, &g_tc_status)) break;
+                    mbar_arrive_expect_tx(&full[s], pbytes + S::kXStage);
+                    const uint32_t* src = p.qd + L.block_word(nb, kb) + (size_t)half * 2 * W * 4;
+                    bulk_g2s(smem + S::kPOff + s * kPackedStageBytes, src, pbytes, &full[s]);
+                }
                 tma_load_2d(smem + S::kXOff + s * S::kXStage, &tmap_x, kb * 128 + half * 64, tok0, &full[s]);
                 ++issued;
             }
+            if (issued < pre) issued = pre;  // prefetched slabs are in flight too
             // drain: every issued stage must have landed before the CTA may exit
             for (int it = (issued > kStages ? issued - kStages : 0); it < issued; ++it) {
                 const int s = it % kStages;
@@ -181,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 32 ? 2 : 1) tc_gemm_kernel(con
                 }
                 if (ok) mma_commit(&d_full[b]);
             }
+            pdl_launch_dependents();  // this CTA issues no more work; let the next grid queue up
             // all MMAs this thread issued must be complete before TMEM is freed
             mma_commit(mma_done);
             const uint64_t t0 = globaltimer();
@@ -369,7 +387,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 template <int NT>
-static cudaError_t launch_nt(const CUtensorMap& tm, const TcParams& prm, const TcPlan& plan, cudaStream_t s) {
+static cudaError_t launch_nt(const CUtensorMap& tm, const TcParams& prm, const TcPlan& plan, cudaStream_t s,
+                             bool pdl) {
     auto kern = tc_gemm_kernel<NT>;
     static int set_for[64];  // shared memory limit raised once per device
     int dev = 0;
@@ -382,12 +401,12 @@ static cudaError_t launch_nt(const CUtensorMap& tm, const TcParams& prm, const T
         set_for[dev] = 1;
     }
     dim3 grid(plan.NB, plan.MT, plan.splits);
-    kern<<<grid, kThreads, plan.smem, s>>>(tm, prm);
-    return cudaGetLastError();
+    return launch_kernel(kern, grid, dim3(kThreads), plan.smem, s, pdl, tm, prm);
 }
 
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
-                      uint16_t* y, int M, int N, int K, void* ws, const TcPlan& plan, cudaStream_t s) {
+                      uint16_t* y, int M, int N, int K, void* ws, const TcPlan& plan, cudaStream_t s,
+                      unsigned flags) {
     auto encode = get_encode();
     if (!encode) return cudaErrorNotSupported;
     CUtensorMap tm;
@@ -415,11 +434,13 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
     prm.NB = plan.NB;
     prm.MT = plan.MT;
     prm.splits = plan.splits;
+    const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
+    prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     switch (plan.NT) {
-        case 16: return launch_nt<16>(tm, prm, plan, s);
-        case 32: return launch_nt<32>(tm, prm, plan, s);
-        case 64: return launch_nt<64>(tm, prm, plan, s);
-        default: return launch_nt<128>(tm, prm, plan, s);
+        case 16: return launch_nt<16>(tm, prm, plan, s, pdl);
+        case 32: return launch_nt<32>(tm, prm, plan, s, pdl);
+        case 64: return launch_nt<64>(tm, prm, plan, s, pdl);
+        default: return launch_nt<128>(tm, prm, plan, s, pdl);
     }
 }
 

@@ -43,6 +43,7 @@ struct GemvParams {
     int cpt;        // chunks per tile = 4 * KB
     long long C;    // total chunks
     int P;          // workers
+    int prefetch;   // weights may be loaded before the preceding grid completes
 };
 
 constexpr int kGemvWG = 4;  // worker warpgroups per CTA
@@ -139,8 +140,19 @@ __global__ void __launch_bounds__(128 * kGemvWG, 1) gemv_kernel(const GemvParams
         const uint32_t* src = p.qd + L.block_word(nb, rem >> 2) + ((size_t)(rem & 3) * W + t) * 4;
         return ld_stream_v4(src);
     };
+    // With static weights the first loads go out before waiting on the
+    // preceding grid; otherwise after it (x, y and the workspace are always
+    // touched only after the wait).
+    if (p.prefetch) {
 #pragma unroll
-    for (int i = 0; i < D; ++i) buf[i] = (c_begin + i < c_end) ? load_chunk(c_begin + i) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < D; ++i) buf[i] = (c_begin + i < c_end) ? load_chunk(c_begin + i) : make_uint4(0, 0, 0, 0);
+    }
+    pdl_wait();
+    if (!p.prefetch) {
+#pragma unroll
+        for (int i = 0; i < D; ++i) buf[i] = (c_begin + i < c_end) ? load_chunk(c_begin + i) : make_uint4(0, 0, 0, 0);
+    }
+    pdl_launch_dependents();  // one wave: the next grid can only start where this one ends
 
     // 2. activations to shared memory, then per-chunk sums
     {
@@ -255,7 +267,7 @@ bool gemv_plan(int M, int N, int K, int sms, GemvPlan* out) {
 }
 
 template <int M>
-static cudaError_t launch_m(const GemvParams& prm, const GemvPlan& plan, cudaStream_t s) {
+static cudaError_t launch_m(const GemvParams& prm, const GemvPlan& plan, cudaStream_t s, bool pdl) {
     constexpr int D = 4;
     auto kern = gemv_kernel<M, D>;
     // the dynamic shared memory limit is raised once per device to the maximum
@@ -271,12 +283,12 @@ static cudaError_t launch_m(const GemvParams& prm, const GemvPlan& plan, cudaStr
         if (e != cudaSuccess) return e;
         set_for[dev] = 1;
     }
-    kern<<<plan.ctas, 128 * kGemvWG, plan.smem, s>>>(prm);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(plan.ctas), dim3(128 * kGemvWG), plan.smem, s, pdl, prm);
 }
 
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
-                        uint16_t* y, int M, int N, int K, void* ws, const GemvPlan& plan, cudaStream_t s) {
+                        uint16_t* y, int M, int N, int K, void* ws, const GemvPlan& plan, cudaStream_t s,
+                        unsigned flags) {
     const Layout L(K, N);
     GemvParams prm;
     prm.x = x;
@@ -294,11 +306,13 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qd, const uint16_t* s
     prm.cpt = 4 * L.KB;
     prm.C = plan.C;
     prm.P = plan.P;
+    const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
+    prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     switch (gemv_mtile(M)) {
-        case 1: return launch_m<1>(prm, plan, s);
-        case 2: return launch_m<2>(prm, plan, s);
-        case 4: return launch_m<4>(prm, plan, s);
-        default: return launch_m<8>(prm, plan, s);
+        case 1: return launch_m<1>(prm, plan, s, pdl);
+        case 2: return launch_m<2>(prm, plan, s, pdl);
+        case 4: return launch_m<4>(prm, plan, s, pdl);
+        default: return launch_m<8>(prm, plan, s, pdl);
     }
 }
 

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "w4a16.h"
+
 namespace w4a16 {
 
 cudaError_t launch_pack(const uint32_t* q, uint32_t* qd, int K, int N, cudaStream_t s);
@@ -18,7 +20,8 @@ struct GemvPlan {
 };
 bool gemv_plan(int M, int N, int K, int sms, GemvPlan* out);
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
-                        uint16_t* y, int M, int N, int K, void* ws, const GemvPlan& plan, cudaStream_t s);
+                        uint16_t* y, int M, int N, int K, void* ws, const GemvPlan& plan, cudaStream_t s,
+                        unsigned flags);
 int gemv_read_status();
 
 // tcgen05 tensor-core GEMM (any M)
@@ -28,7 +31,26 @@ struct TcPlan {
 };
 bool tc_plan(int M, int N, int K, int sms, TcPlan* out);
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
-                      uint16_t* y, int M, int N, int K, void* ws, const TcPlan& plan, cudaStream_t s);
+                      uint16_t* y, int M, int N, int K, void* ws, const TcPlan& plan, cudaStream_t s,
+                      unsigned flags);
+
+// Launch `kern` with an optional programmatic-stream-serialization attribute.
+template <typename Kern, typename... Args>
+cudaError_t launch_kernel(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 int tc_read_status();
 
 // failure-detection self-test

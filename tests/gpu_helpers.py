@@ -54,9 +54,10 @@ class Device:
         self.x, self.qw, self.scales, self.qzeros = w.to_device(prob)
         self.qd = w.w4a16_pack(self.qw)
 
-    def run(self, path=0, x=None, workspace=None) -> torch.Tensor:
+    def run(self, path=0, x=None, workspace=None, flags=None, out=None) -> torch.Tensor:
         x = self.x if x is None else x
-        return self.w.w4a16_gemm(x, self.qd, self.scales, self.qzeros, path=path, workspace=workspace)
+        return self.w.w4a16_gemm(x, self.qd, self.scales, self.qzeros, path=path, workspace=workspace,
+                                 flags=flags, out=out)
 
 
 def sample_indices(M: int, N: int, count: int, seed: int):

@@ -259,3 +259,43 @@ def test_one_workspace_across_shapes_and_paths():
         d = Device(p)
         y = d.run(path, workspace=ws)
         check_sampled(d, y, 2000, seed=i, what=f"shared workspace {shape} M={M}")
+
+
+# ---- launch flags: programmatic dependent launch ------------------------------
+
+@pytest.mark.parametrize("flags", [0, 1, 3])
+@pytest.mark.parametrize("shape,M,path", [("qkv", 1, GEMV), ("down", 8, GEMV), ("o_proj", 16, TC),
+                                          ("gate_up", 64, TC), ("down", 300, TC)])
+def test_launch_flags_same_result(flags, shape, M, path):
+    """Every flag combination gives the same bits (the flags change launch
+    overlap only) and matches the oracle."""
+    p = wi.generate_named(shape, M, 30)
+    d = Device(p)
+    base = d.run(path, flags=0)
+    y = d.run(path, flags=flags)
+    torch.cuda.synchronize()
+    assert torch.equal(base.view(torch.int16), y.view(torch.int16))
+    check_sampled(d, y, 1500, seed=2, what=f"flags={flags} {shape} M={M}")
+
+
+@pytest.mark.parametrize("M,path", [(1, GEMV), (4, GEMV), (16, TC), (256, TC)])
+@pytest.mark.parametrize("flags", [1, 3])
+def test_chained_layers_respect_order(M, path, flags):
+    """Layer 2 reads layer 1's output as its x.  Launched back to back as
+    programmatic dependents, layer 2 must still see the finished y1: y1's
+    buffer starts as NaN, so reading it early would show."""
+    import int4_weight_only_gemm_gb300 as w
+    p1 = wi.generate(M, 1024, 2048, seed=41)
+    p2 = wi.generate(M, 2048, 512, seed=42)
+    d1, d2 = Device(p1), Device(p2)
+    for _ in range(3):
+        y1 = torch.full((M, 2048), float("nan"), dtype=torch.bfloat16, device="cuda")
+        y2 = torch.full((M, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        d1.run(path, flags=flags, out=y1)
+        d2.run(path, x=y1, flags=flags, out=y2)
+        torch.cuda.synchronize()
+        x2 = bf16_bits(y1)
+        assert np.all(np.isfinite(oracle.bf16_to_f64(x2[:1])))
+        ref = oracle.gemm(x2, p2.qweight, p2.scales, p2.qzeros)
+        check_close(bf16_to_f64(y2), ref, f"chain M={M} flags={flags}")
+    assert w.w4a16_last_device_status() == 0
