@@ -180,6 +180,35 @@ int w4a16_last_device_status(w4a16_stream_t stream);
  */
 int w4a16_selftest_wait_timeout(long long wait_ns, w4a16_stream_t stream);
 
+/* Size of the scratch array built into the library for w4a16_gemm_noalloc:
+ * 4 MiB, held on every GPU that loads the library until the process exits. */
+#define W4A16_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * The GEMM for M <= 8 (the split-K GEMV) with no allocation and no workspace
+ * argument.  The pages have no counterpart to this call: it exists for callers
+ * that may not allocate device memory -- a plugin inside a runtime that plans
+ * all device memory itself, code under a locked-down or byte-budgeted
+ * allocator -- and so cannot hand the regular entry points the workspace they
+ * need for split-K partial sums.  The scratch is instead a fixed array compiled
+ * into the library (W4A16_NOALLOC_SCRATCH_BYTES).  The caller still passes x,
+ * the packed weights, scales, zeros and y, as for w4a16_gemm.
+ *   - Arguments and errors as w4a16_gemm.  M > 8 gives W4A16_EUNSUPPORTED; a
+ *     problem whose scratch need exceeds the array gives W4A16_EWORKSPACE.
+ *     Nothing is launched then.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents: each call first clears the arrival counters it uses (a memset
+ *     on `stream`), and calls that may overlap on the GPU (other streams, other
+ *     host threads) race on it, so the caller must serialise them.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+int w4a16_gemm_noalloc(const void *x, const uint32_t *qweight_dev, const void *scales,
+                       const uint32_t *qzeros, int M, int N, int K, int group, void *y,
+                       w4a16_stream_t stream);
+
 /* Number of kernel launches the library has issued in this process. */
 uint64_t w4a16_launch_count(void);
 
