@@ -103,34 +103,50 @@ W4A16_DEVICE bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
 
 // Bounded wait for the phase with the given parity to complete.  `abort` is a
 // shared flag: once any thread of the CTA has given up, the others stop
-// waiting at once.  Returns false on timeout or abort.
+// waiting at once.  The clock is read only every 1024 polls, so a wait that
+// succeeds soon costs nothing but the polls.  Returns false on timeout or abort.
 W4A16_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
                             uint64_t limit_ns = kWaitNs) {
     const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait(a, parity)) return true;
-    const uint64_t t0 = globaltimer();
+    if (abort && *abort) return false;
+    uint64_t t0 = 0;
     for (uint32_t i = 0; i < kWaitSpins; ++i) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((i & 63) == 63) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > limit_ns) {
-                *abort = 1;
+        if ((i & 1023) == 1023) {
+            if (abort && *abort) return false;
+            const uint64_t now = globaltimer();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > limit_ns) {
+                if (abort) *abort = 1;
                 atomicExch(status, (int)W4A16_ETIMEOUT);
                 return false;
             }
         }
     }
-    *abort = 1;
+    if (abort) *abort = 1;
     atomicExch(status, (int)W4A16_ETIMEOUT);
     return false;
 }
 
-// Warp-uniform bounded wait: lane 0 polls, every lane gets the same answer, so
-// the warp-collective tcgen05 instructions that follow never diverge.
+// Warp-uniform bounded wait: every lane waits (so every lane acquires the
+// phase), then the warp agrees on the outcome, so the warp-collective tcgen05
+// instructions that follow never diverge.
 W4A16_DEVICE bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
-    int ok = 0;
-    if (lane_id() == 0) ok = mbar_wait(bar, parity, abort, status) ? 1 : 0;
-    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+    const bool ok = mbar_wait(bar, parity, abort, status);
+    return __all_sync(0xFFFFFFFFu, ok) != 0;
+}
+
+// One lane of a converged warp is elected (the same lane for every caller).
+W4A16_DEVICE bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\t"
+        "elect.sync rx|px, %1;\n\t"
+        "selp.b32 %0, 1, 0, px;\n\t}"
+        : "=r"(pred)
+        : "r"(0xFFFFFFFFu));
+    return pred != 0;
 }
 
 // AND of `pred` over the `count` threads of named barrier `id` (all must arrive).
@@ -145,6 +161,18 @@ W4A16_DEVICE bool bar_and(int id, int count, bool pred) {
         : "r"((uint32_t)pred), "r"(id), "r"(count)
         : "memory");
     return r != 0;
+}
+
+// explicit shared-memory loads (32-bit shared addresses)
+W4A16_DEVICE uint4 lds_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+W4A16_DEVICE uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
 }
 
 // ---------------------------------------------------------------------------
@@ -163,6 +191,24 @@ W4A16_DEVICE void tma_load_2d(void* smem_dst, const void* tmap, int x, int y, ui
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
         "[%4];" ::"r"(smem_u32(smem_dst)),
         "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared (completion tracked below)
+W4A16_DEVICE void cp_async_4(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+// The mbarrier's current phase also waits for this thread's earlier cp.async
+// copies (net-zero change to the arrival count).
+W4A16_DEVICE void cp_async_mbar_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+W4A16_DEVICE void tma_load_3d(void* smem_dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
 

@@ -1,4 +1,4 @@
-// Tensor-core W4A16 GEMM on sm_103a: TMA + tcgen05 with the weights in TMEM.
+// Tensor-core W4A16 GEMM on sm_103a: persistent, TMA + tcgen05, weights in TMEM.
 //
 // y[m][n] = sum_g s[g][n] * sum_{k in g} x[m][k] (q[k][n] - z[g][n]), g = 128
 // rows: the INT4 linear layer of "Quantize the Target, Quantize the Drafter"
@@ -7,24 +7,29 @@
 // for the 16-token verify blocks (DFlash block size 16) and for prefill.
 //
 // Orientation (swap AB): the MMA's M = 128 rows are 128 output columns n,
-// its N = NT columns are NT tokens.  D[n][token] lives in tensor memory.
+// its N = NT columns are NT tokens.  Work units are (column tile, token tile,
+// K split); each CTA walks units blockIdx.x, +gridDim.x, ... and all of its
+// roles walk the same sequence of (unit, group) pairs, numbered q = 0, 1, ...
+// One pipeline stage carries one group of 128 rows of K.
 //
-//  * producer warp: per 64-row K stage, one bulk copy of the packed weight
-//    slab (4 KB, contiguous in the device layout) and one TMA tile of x
-//    (NT tokens x 64 bf16, 128-byte swizzle) into a 4-deep shared ring;
-//  * dequant warpgroup: thread t turns its column's 8 words into 32 bfloat16
-//    pairs (q - z), exact small integers (mask-and-or to 128 + q, subtract
-//    128 + z), and writes them to tensor memory as the MMA's A operand
-//    (tcgen05.st), so the dequantized weights never touch shared memory;
-//  * MMA warp: one thread issues tcgen05.mma kind::f16 (A from TMEM, B = x
-//    from shared memory), 4 per stage; each group of 128 rows accumulates
-//    into its own D buffer (two, double-buffered);
-//  * rescale warpgroup: per group, reads D_g with tcgen05.ld and adds
-//    s[g][n] * D_g into f32 registers -- the binary16 scale is applied in
-//    f32, never rounded to bfloat16 -- then writes bf16 y (or split-K partials).
+//  * producer warp: per group, into ring stage q % SS: the packed weight slab
+//    (bulk copy, 8 KB for a full tile), the group's scales (bulk copy), its
+//    zero-point words (4-byte cp.async) and the x tile (two TMA boxes of
+//    NT x 64 bf16, 128-byte swizzle), all completing one barrier;
+//  * two dequant warpgroups, taking alternate groups: thread t turns column
+//    t's 16 words into 64 bfloat16 pairs (q - z) -- exact small integers:
+//    mask-and-or to 128 + q, subtract 128 + z -- and writes them to tensor
+//    memory as the MMA's A operand (tcgen05.st, buffer q % 4); after a
+//    warpgroup barrier one of its threads issues the group's 8 tcgen05.mma
+//    kind::f16 (A from TMEM, B = x from shared memory) into D buffer q % 2;
+//  * rescale warpgroup(s): per group, reads D with tcgen05.ld and adds
+//    s[g][n] * D into f32 registers (the binary16 scale is applied in f32,
+//    never rounded to bfloat16); at a unit's end writes bf16 y, or split-K
+//    partials reduced in fixed order by the last CTA to arrive.
 //
-// Every wait is bounded (see common.cuh); on a timeout the CTA stops, waits
-// for its own copies in flight, frees its tensor memory and returns.
+// Every wait is bounded (common.cuh).  After a timeout every role keeps
+// walking its loop without doing work, so all barriers still meet; the CTA
+// then drains its copies and MMAs, frees its tensor memory and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -35,11 +40,6 @@ namespace w4a16 {
 
 static __device__ int g_tc_status;
 
-constexpr int kStages = 4;         // K stages of 64 rows in the ring
-constexpr int kStageK = 64;
-constexpr int kPackedStageBytes = 128 * kStageK / 2;  // 4 KB
-constexpr int kThreads = 320;      // 10 warps: producer, MMA, 4 dequant, 4 rescale
-
 struct TcParams {
     const uint32_t* qd;
     const uint16_t* scales;
@@ -48,325 +48,463 @@ struct TcParams {
     uint32_t* counters;
     float* partials;
     int M, N, K, G;
-    int NB, MT;      // column tiles, token tiles
-    int splits;      // K splits (groups divided evenly)
+    int NB, MT, splits;
+    int units;       // NB * MT * splits
     int prefetch;    // weights may be loaded before the preceding grid completes
 };
 
+// Configuration per token-tile width NT (one CTA per SM).
 template <int NT>
-struct TcSmem {
-    static constexpr int kXStage = NT * 128;  // NT rows x 64 bf16
+struct TcCfg {
+    static constexpr int R = NT >= 128 ? 2 : 1;          // rescale warpgroups, each owning NT/R columns
+    static constexpr int SS = NT <= 16 ? 12 : NT <= 32 ? 10 : 4;  // shared-memory ring stages
+    static constexpr int SA = NT <= 32 ? 4 : 2;          // A buffers in tensor memory (q % SA)
+    static constexpr int NDB = ((512 - SA * 64) / NT) < 8 ? ((512 - SA * 64) / NT) : 8;  // D accumulator ring
+    static constexpr int kDone = 16;                     // ring of "MMAs of group q done" barriers
+    static constexpr int kDeqWG = NT <= 32 ? 4 : 2;      // dequant warpgroups, taking groups q % kDeqWG
+    static constexpr int kDeqWarps = 4 * kDeqWG;
+    static constexpr int kResWarp0 = kDeqWarps;          // rescale warpgroups follow
+    static constexpr int kMmaWarp = kDeqWarps + 4 * R;   // then the MMA warp (the only tcgen05.mma issuer)
+    static constexpr int kProdWarp = kMmaWarp + 1;       // weight producer (also owns TMEM)
+    static constexpr int kXWarp = kProdWarp + 1;         // activation producer
+    static constexpr int kThreads = 32 * (kXWarp + 1);
+    static_assert(SS <= kDone && SA <= kDone && NDB <= kDone, "barrier ring too short for the phase parity");
+    // shared memory, from a 1024-byte aligned base
+    static constexpr int kXStage = NT * 256;             // two swizzled boxes of NT rows x 128 bytes
     static constexpr int kXOff = 0;
-    static constexpr int kPOff = kXOff + kStages * kXStage;
-    static constexpr int kBarOff = kPOff + kStages * kPackedStageBytes;
-    static constexpr int kBytes = kBarOff + 256;
-    static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
-    // tensor memory columns: D double buffer + A ring (32 columns per stage)
-    static constexpr int kTmemD = 0;
-    static constexpr int kTmemA = 2 * NT;
-    static constexpr int kTmemCols = (2 * NT + kStages * 32) <= 256 ? 256 : 512;
+    static constexpr int kPOff = kXOff + SS * kXStage;   // packed weights, 8 KB per stage
+    static constexpr int kZOff = kPOff + SS * 8192;      // zero words, 64 bytes per stage
+    static constexpr int kBarOff = kZOff + SS * 64;
+    static constexpr int kBytes = kBarOff + 1024;
+    static constexpr int kAlloc = kBytes + 1024;         // slack for the alignment
+    // tensor memory: SA A-buffers of 64 columns, then the D ring of NDB x NT columns
+    static constexpr int kTmemA = 0;
+    static constexpr int kTmemD = SA * 64;
+    static constexpr int kTmemUsed = SA * 64 + NDB * NT;
+    static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
+    static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+    static_assert(kTmemUsed <= 512, "tensor memory budget");
 };
 
+struct UnitInfo {
+    int nb, mb, split, g0, g1;
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const TcParams& p, int u) {
+    UnitInfo r;
+    r.nb = u % p.NB;
+    const int rest = u / p.NB;
+    r.mb = rest % p.MT;
+    r.split = rest / p.MT;
+    r.g0 = (int)((long long)r.split * p.G / p.splits);
+    r.g1 = (int)((long long)(r.split + 1) * p.G / p.splits);
+    return r;
+}
+
+W4A16_DEVICE void tmem_st_x32(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
 template <int NT>
-__global__ void __launch_bounds__(kThreads, NT <= 32 ? 2 : 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                                                              const TcParams p) {
-    using S = TcSmem<NT>;
+__global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcParams p) {
+    using C = TcCfg<NT>;
+    constexpr int SS = C::SS;
+    constexpr int SA = C::SA;
+    constexpr int R = C::R;
+    constexpr int ND = C::kDone;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
-    uint64_t* full = bars;                   // [kStages] tx: packed + x arrived
-    uint64_t* a_full = bars + kStages;       // [kStages] A stage written to TMEM
-    uint64_t* empty = bars + 2 * kStages;    // [kStages] MMA done with the stage
-    uint64_t* d_full = bars + 3 * kStages;   // [2] group accumulated
-    uint64_t* d_empty = d_full + 2;          // [2] group read by rescale warps
-    uint64_t* mma_done = d_empty + 2;        // [1] every issued MMA has finished
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint64_t* full = bars;                 // [SS] stage landed (transactions + cp.async)
+    uint64_t* done = bars + SS;            // [ND] all MMAs of group q finished: done[q % ND]
+    uint64_t* a_full = done + ND;          // [SA] A buffer q % SA written (4 dequant warps)
+    uint64_t* d_empty = a_full + SA;       // [NDB] D buffer read by every rescale warp
+    uint64_t* mma_done = d_empty + C::NDB; // [1] every MMA of the CTA finished
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     int* sh_last = const_cast<int*>(abort_flag) + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int nb = blockIdx.x, mb = blockIdx.y, split = blockIdx.z;
     const Layout L(p.K, p.N);
-    const int W = L.width(nb);
-    const int g_begin = (int)((long long)split * p.G / p.splits);
-    const int g_end = (int)((long long)(split + 1) * p.G / p.splits);
-    const int n_groups = g_end - g_begin;
-    const int n_stages = 2 * n_groups;
-    const int tok0 = mb * NT;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&a_full[i], 4);
-            mbar_init(&empty[i], 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&d_full[i], 1);
-            mbar_init(&d_empty[i], 4);
-        }
+        for (int i = 0; i < SS; ++i) mbar_init(&full[i], 2);  // one arrival per producer warp
+        for (int i = 0; i < ND; ++i) mbar_init(&done[i], 1);
+        for (int i = 0; i < SA; ++i) mbar_init(&a_full[i], 4);
+        for (int i = 0; i < C::NDB; ++i) mbar_init(&d_empty[i], 4 * R);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
-        tmem_alloc(tmem_holder, S::kTmemCols);
+    if (warp == C::kProdWarp) {
+        tmem_alloc(tmem_holder, C::kTmemCols);
         tmem_relinquish();
+        if (lane == 0) prefetch_tmap(&tmap_x);
     }
-    if (warp == 0 && lane == 0) prefetch_tmap(&tmap_x);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    // everything but the producer thread reads global memory only after the
-    // preceding grid has completed (the producer waits in its own loop)
-    if (!(warp == 0 && lane == 0)) pdl_wait();
+    if (warp != C::kProdWarp && warp != C::kXWarp) pdl_wait();  // producers wait in their own loops
 
-    if (warp == 0) {
-        // ---------------- producer ----------------
-        if (lane == 0) {
-            int issued = 0;
-            const uint32_t pbytes = (uint32_t)W * 32;  // W columns x 8 words
-            // with static weights, the first ring's weight slabs go out before
-            // waiting on the preceding grid; x only after it
-            const int pre = p.prefetch ? (n_stages < kStages ? n_stages : kStages) : 0;
-            for (int it = 0; it < pre; ++it) {
-                const int kb = g_begin + (it >> 1);
-                mbar_arrive_expect_tx(&full[it], pbytes + S::kXStage);
-                bulk_g2s(smem + S::kPOff + it * kPackedStageBytes,
-                         p.qd + L.block_word(nb, kb) + (size_t)(it & 1) * 2 * W * 4, pbytes, &full[it]);
-            }
-            pdl_wait();
-            for (int it = 0; it < n_stages; ++it) {
-                const int s = it % kStages;
-                const int use = it / kStages;
-                const int kb = g_begin + (it >> 1);
-                const int half = it & 1;
-                if (it >= pre) {
-                    if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, abort_flag, &g_tc_status)) break;
-                    mbar_arrive_expect_tx(&full[s], pbytes + S::kXStage);
-                    const uint32_t* src = p.qd + L.block_word(nb, kb) + (size_t)half * 2 * W * 4;
-                    bulk_g2s(smem + S::kPOff + s * kPackedStageBytes, src, pbytes, &full[s]);
-                }
-                tma_load_2d(smem + S::kXOff + s * S::kXStage, &tmap_x, kb * 128 + half * 64, tok0, &full[s]);
-                ++issued;
-            }
-            if (issued < pre) issued = pre;  // prefetched slabs are in flight too
-            // drain: every issued stage must have landed before the CTA may exit
-            for (int it = (issued > kStages ? issued - kStages : 0); it < issued; ++it) {
-                const int s = it % kStages;
-                const int use = it / kStages;
-                uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(smem_u32(&full[s]), use & 1)) {
-                    if (globaltimer() - t0 > kWaitNs) {
-                        atomicExch(&g_tc_status, (int)W4A16_ETIMEOUT);
-                        break;
+    if (warp == C::kProdWarp) {
+        // ------------------------------------------------ weight producer
+        // Per group, into ring stage q % SS: the packed weight slab and the
+        // zero-point words.  The zero words are 16-byte aligned when
+        // N % 32 == 0 and then come in one bulk copy; otherwise lane 0 fetches
+        // them with 4-byte async copies.
+        int q = 0, issued = 0;
+        bool ok = true;
+        const bool zbulk = p.N % 32 == 0;
+        // This warp touches only weights and zeros: with static weights it
+        // never waits on the preceding grid, otherwise once before any load.
+        if (!p.prefetch) pdl_wait();
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+            const UnitInfo ui = unit_info(p, u);
+            const int W = L.width(ui.nb);
+            const uint32_t wbytes = (uint32_t)W * 64;
+            const uint32_t zbytes = zbulk ? (uint32_t)(W / 2) : 0u;
+            const uint32_t* wsrc = p.qd + L.block_word(ui.nb, ui.g0);
+            const uint32_t* zsrc = p.qzeros + (size_t)ui.g0 * (p.N / 8) + 16 * ui.nb;
+            for (int g = ui.g0; g < ui.g1; ++g, ++q, wsrc += W * 16, zsrc += p.N / 8) {
+                const int s = q % SS;
+                // stage s is free once the MMAs of group q - SS are done
+                if (ok && q >= SS &&
+                    !mbar_wait_warp(&done[(q - SS) % ND], ((q - SS) / ND) & 1, abort_flag, &g_tc_status))
+                    ok = false;
+                if (ok) {
+                    if (lane == 0) {
+                        if (!zbulk) {
+                            for (int i = 0; i < W / 8; ++i) cp_async_4(smem + C::kZOff + s * 64 + i * 4, zsrc + i);
+                            cp_async_mbar_arrive(&full[s]);
+                        }
+                        mbar_arrive_expect_tx(&full[s], wbytes + zbytes);
+                        bulk_g2s(smem + C::kPOff + s * 8192, wsrc, wbytes, &full[s]);
+                        if (zbulk) bulk_g2s(smem + C::kZOff + s * 64, zsrc, zbytes, &full[s]);
                     }
+                    __syncwarp();
+                    issued = q + 1;
                 }
             }
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, NT);
-            bool ok = true;
-            for (int gi = 0; gi < n_groups && ok; ++gi) {
-                const int b = gi & 1;
-                const int buse = gi >> 1;
-                if (buse > 0 && !mbar_wait(&d_empty[b], (buse - 1) & 1, abort_flag, &g_tc_status)) break;
-                tc_fence_after();
-                for (int h = 0; h < 2; ++h) {
-                    const int it = 2 * gi + h;
-                    const int s = it % kStages;
-                    const int use = it / kStages;
-                    if (!mbar_wait(&full[s], use & 1, abort_flag, &g_tc_status) ||
-                        !mbar_wait(&a_full[s], use & 1, abort_flag, &g_tc_status)) {
-                        ok = false;
-                        break;
+        // drain: every stage armed must land before the CTA may exit
+        for (int i = issued > SS ? issued - SS : 0; i < issued; ++i)
+            (void)mbar_wait(&full[i % SS], (i / SS) & 1, nullptr, &g_tc_status);
+    } else if (warp == C::kXWarp) {
+        // -------------------------------------------- activation producer
+        // Per group: x[tile tokens][128 rows of K] with one 3-D TMA (two
+        // 64-wide, 128-byte swizzled slabs).  Always after the preceding grid.
+        pdl_wait();
+        int q = 0, issued = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+            const UnitInfo ui = unit_info(p, u);
+            for (int g = ui.g0; g < ui.g1; ++g, ++q) {
+                const int s = q % SS;
+                if (ok && q >= SS &&
+                    !mbar_wait_warp(&done[(q - SS) % ND], ((q - SS) / ND) & 1, abort_flag, &g_tc_status))
+                    ok = false;
+                if (ok) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)C::kXStage);
+                        tma_load_3d(smem + C::kXOff + s * C::kXStage, &tmap_x, 0, ui.mb * NT, 2 * g, &full[s]);
                     }
-                    tc_fence_after();
-                    const uint32_t xaddr = smem_u32(smem + S::kXOff + s * S::kXStage);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t bdesc = smem_desc_sw128(xaddr + kk * 32);
-                        const uint32_t a_tmem = tmem + S::kTmemA + s * 32 + kk * 8;
-                        const uint32_t d_tmem = tmem + S::kTmemD + b * NT;
-                        mma_bf16_ts(d_tmem, a_tmem, bdesc, idesc, (h | kk) ? 1u : 0u);
-                    }
-                    mma_commit(&empty[s]);
-                }
-                if (ok) mma_commit(&d_full[b]);
-            }
-            pdl_launch_dependents();  // this CTA issues no more work; let the next grid queue up
-            // all MMAs this thread issued must be complete before TMEM is freed
-            mma_commit(mma_done);
-            const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(smem_u32(mma_done), 0)) {
-                if (globaltimer() - t0 > kWaitNs) {
-                    atomicExch(&g_tc_status, (int)W4A16_ETIMEOUT);
-                    break;
+                    __syncwarp();
+                    issued = q + 1;
                 }
             }
         }
-    } else if (warp < 6) {
-        // ---------------- dequant warpgroup (warps 2..5) ----------------
-        const int quad = warp & 3;          // TMEM lane quadrant this warp may access
-        const int t = quad * 32 + lane;     // row of A = column of the tile
-        const int n = nb * 128 + t;
-        const bool valid = t < W;
+        for (int i = issued > SS ? issued - SS : 0; i < issued; ++i)
+            (void)mbar_wait(&full[i % SS], (i / SS) & 1, nullptr, &g_tc_status);
+    } else if (warp < C::kDeqWarps) {
+        // ------------------------------------------------------------ dequant
+        const int h = warp >> 2;              // warpgroup: takes groups q with q % kDeqWG == h
+        const int quad = warp & 3;            // TMEM lane quadrant
+        const int t = quad * 32 + lane;       // A row = tile column
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        uint32_t zz = 0x43004300u;
-        for (int it = 0; it < n_stages; ++it) {
-            const int s = it % kStages;
-            const int use = it / kStages;
-            const int kb = g_begin + (it >> 1);
-            if ((it & 1) == 0 && valid) {
-                const uint32_t zw = __ldg(p.qzeros + (size_t)kb * (p.N / 8) + (n >> 3));
-                const uint32_t z = (zw >> (4 * (n & 7))) & 0xFu;
-                zz = 0x43004300u | z | (z << 16);  // bfloat16 pair (128 + z, 128 + z)
-            }
-            if (!mbar_wait_warp(&full[s], use & 1, abort_flag, &g_tc_status)) break;
-            uint32_t a[32];
-            if (valid) {
-                const uint4* src = reinterpret_cast<const uint4*>(smem + S::kPOff + s * kPackedStageBytes);
+        int q = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+            const UnitInfo ui = unit_info(p, u);
+            const int W = L.width(ui.nb);
+            // columns beyond a ragged tile read column W-1; their A rows only
+            // feed D rows that are never written out
+            const int tc = t < W ? t : W - 1;
+            for (int g = ui.g0; g < ui.g1; ++g, ++q) {
+                if ((q % C::kDeqWG) != h) continue;
+                const int s = q % SS;
+                if (ok && !mbar_wait_warp(&full[s], (q / SS) & 1, abort_flag, &g_tc_status)) ok = false;
+                // first half computed before waiting for the A buffer, so the
+                // ALU work overlaps the previous group's MMAs
+                const uint32_t zs = smem_u32(smem + C::kZOff + s * 64);
+                const uint32_t src = smem_u32(smem + C::kPOff + s * 8192);
+                uint32_t zz = 0x43004300u;
+                uint32_t a[32];
+                auto dequant_half = [&](int half) {
 #pragma unroll
-                for (int cl = 0; cl < 2; ++cl) {
-                    const uint4 v = src[cl * W + t];
-                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                    for (int cl = 0; cl < 2; ++cl) {
+                        const uint4 v = lds_v4(src + (uint32_t)(((2 * half + cl) * W + tc) * 16));
+                        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
+                        for (int j = 0; j < 4; ++j)
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) a[16 * cl + 4 * j + q] = bf16x2_sub(magic_pair(wv[j], q), zz);
+                            for (int pp = 0; pp < 4; ++pp) a[16 * cl + 4 * j + pp] = bf16x2_sub(magic_pair(wv[j], pp), zz);
+                    }
+                };
+                if (ok) {
+                    const uint32_t z = (lds_u32(zs + (uint32_t)((tc >> 3) * 4)) >> (4 * (tc & 7))) & 0xFu;
+                    zz = 0x43004300u | z | (z << 16);  // bfloat16 pair (128 + z, 128 + z)
+                    dequant_half(0);
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) a[i] = 0u;
+                // A buffer q % SA is free once the MMAs of group q - SA are done
+                if (ok && q >= SA &&
+                    !mbar_wait_warp(&done[(q - SA) % ND], ((q - SA) / ND) & 1, abort_flag, &g_tc_status))
+                    ok = false;
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t abase = tmem + lane_base + C::kTmemA + (q % SA) * 64;
+                    tmem_st_x32(abase, a);
+                    tmem_wait_st();  // the registers of the first half are reused below
+                    dequant_half(1);
+                    tmem_st_x32(abase + 32, a);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_full[q % SA]);
+                }
+                if (!ok) *abort_flag = 1;
             }
-            const uint32_t abase = tmem + lane_base + S::kTmemA + s * 32;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t v8[8] = {a[8 * c], a[8 * c + 1], a[8 * c + 2], a[8 * c + 3],
-                                        a[8 * c + 4], a[8 * c + 5], a[8 * c + 6], a[8 * c + 7]};
-                tmem_st_x8(abase + 8 * c, v8);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[s]);
         }
+    } else if (warp == C::kMmaWarp) {
+        // ------------------------------------------------------------ MMA issue
+        // The one warp of the CTA that issues tcgen05.mma (an elected lane).
+        // It needs only the flat group index q, and takes two groups a pass
+        // (their waits, then their 16 MMAs), halving its per-group overhead.
+        constexpr uint32_t idesc = idesc_bf16_f32(128, NT);
+        int Q = 0;  // groups this CTA processes
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+            const UnitInfo ui = unit_info(p, u);
+            Q += ui.g1 - ui.g0;
+        }
+        bool ok = true;
+        for (int q0 = 0; q0 < Q; q0 += 2) {
+            const int nq = Q - q0 < 2 ? Q - q0 : 2;
+            for (int i = 0; i < nq; ++i) {
+                const int q = q0 + i;
+                if (ok && !mbar_wait_warp(&a_full[q % SA], (q / SA) & 1, abort_flag, &g_tc_status)) ok = false;
+                // D buffer q % NDB is free once every rescale warp has read group q - NDB
+                if (ok && q >= C::NDB &&
+                    !mbar_wait_warp(&d_empty[q % C::NDB], ((q / C::NDB) - 1) & 1, abort_flag, &g_tc_status))
+                    ok = false;
+            }
+            if (ok) {
+                tc_fence_after();
+                if (elect_one()) {
+                    for (int i = 0; i < nq; ++i) {
+                        const int q = q0 + i;
+                        const uint32_t xaddr = smem_u32(smem + C::kXOff + (q % SS) * C::kXStage);
+                        const uint32_t a_tmem = tmem + C::kTmemA + (q % SA) * 64;
+                        const uint32_t d_tmem = tmem + C::kTmemD + (q % C::NDB) * NT;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t bdesc = smem_desc_sw128(xaddr + (kk >> 2) * (NT * 128) + (kk & 3) * 32);
+                            mma_bf16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&done[q % ND]);
+                    }
+                }
+                __syncwarp();
+            }
+            if (!ok) *abort_flag = 1;
+        }
+        pdl_launch_dependents();  // this CTA issues no more tensor work
+        // every MMA issued must be complete before TMEM is freed
+        if (elect_one()) mma_commit(mma_done);
+        __syncwarp();
+        (void)mbar_wait(mma_done, 0, nullptr, &g_tc_status);
     } else {
-        // ---------------- rescale / epilogue warpgroup (warps 6..9) ----------------
+        // ------------------------------------------------------- rescale + epilogue
+        const int r = (warp - C::kResWarp0) >> 2;  // rescale warpgroup: owns columns [r*CW, (r+1)*CW)
         const int quad = warp & 3;
         const int t = quad * 32 + lane;
-        const int n = nb * 128 + t;
-        const bool valid = t < W;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        float acc[NT];
+        constexpr int CW = NT / R;                 // columns (tokens) per rescale warpgroup
+        constexpr int kBatch = CW < 32 ? CW : (CW >= 64 ? 16 : 32);  // columns read from TMEM per wait
+        const int rt = r * 128 + t;                // thread index among the rescale warpgroups
+        float2 acc[CW / 2];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) acc[j] = 0.f;
-        float sc = valid ? f16_bits_to_f32(__ldg(p.scales + (size_t)g_begin * p.N + n)) : 0.f;
+        for (int j = 0; j < CW / 2; ++j) acc[j] = make_float2(0.f, 0.f);
+        // scales of this thread's column for the next groups, loaded ahead of use
+        int lq_u = blockIdx.x, lq_g = -1;  // load cursor over (unit, group)
+        int lq_nb = 0, lq_g1 = 0;
+        auto next_scale = [&]() -> float {
+            if (lq_u >= p.units) return 0.f;
+            if (lq_g < 0 || lq_g >= lq_g1) {  // first call or past the unit's last group
+                if (lq_g >= 0) {
+                    lq_u += gridDim.x;
+                    if (lq_u >= p.units) return 0.f;
+                }
+                const UnitInfo ui = unit_info(p, lq_u);
+                lq_nb = ui.nb;
+                lq_g = ui.g0;
+                lq_g1 = ui.g1;
+            }
+            const int W = L.width(lq_nb);
+            const int tc = t < W ? t : W - 1;
+            const float v = f16_bits_to_f32(__ldg(p.scales + (size_t)lq_g * p.N + 128 * lq_nb + tc));
+            ++lq_g;
+            return v;
+        };
+        float sr0 = next_scale(), sr1 = next_scale(), sr2 = next_scale(), sr3 = next_scale();
+        int q = 0;
         bool ok = true;
-        for (int gi = 0; gi < n_groups; ++gi) {
-            const int b = gi & 1;
-            const int buse = gi >> 1;
-            const float sc_next =
-                (valid && gi + 1 < n_groups) ? f16_bits_to_f32(__ldg(p.scales + (size_t)(g_begin + gi + 1) * p.N + n))
-                                             : 0.f;
-            if (!mbar_wait_warp(&d_full[b], buse & 1, abort_flag, &g_tc_status)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t dbase = tmem + lane_base + S::kTmemD + b * NT;
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+            const UnitInfo ui = unit_info(p, u);
+            const int W = L.width(ui.nb);
+            for (int g = ui.g0; g < ui.g1; ++g, ++q) {
+                const int b = q % C::NDB;
+                if (ok && !mbar_wait_warp(&done[q % ND], (q / ND) & 1, abort_flag, &g_tc_status)) ok = false;
+                if (ok) {
+                    tc_fence_after();
+                    const float2 sc2 = make_float2(sr0, sr0);
+                    const uint32_t dbase = tmem + lane_base + C::kTmemD + b * NT + r * CW;
 #pragma unroll
-            for (int c = 0; c < NT / 16; ++c) {
-                uint32_t v[16];
-                tmem_ld_x16(dbase + 16 * c, v);
-                tmem_wait_ld();
+                    for (int c0 = 0; c0 < CW; c0 += kBatch) {
+                        uint32_t v[kBatch];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[16 * c + i] = fmaf(sc, __uint_as_float(v[i]), acc[16 * c + i]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&d_empty[b]);
-            sc = sc_next;
-        }
-        // every rescale thread reaches this barrier, failed or not, and they
-        // agree on whether to write anything
-        if (bar_and(1, 128, ok)) {
-            const int tile = nb * p.MT + mb;
-            if (p.splits == 1) {
-                if (valid) {
+                        for (int c = 0; c < kBatch; c += 16)
+                            tmem_ld_x16(dbase + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(v + c));
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < NT; ++j)
-                        if (tok0 + j < p.M) p.y[(size_t)(tok0 + j) * p.N + n] = f32_to_bf16_rn(acc[j]);
-                }
-            } else {
-                float* part = p.partials + ((size_t)tile * p.splits + split) * NT * 128;
-#pragma unroll
-                for (int j = 0; j < NT; ++j) part[j * 128 + t] = acc[j];
-                __threadfence();
-                asm volatile("bar.sync 2, 128;" ::: "memory");
-                if (t == 0) {
-                    const unsigned old = atomicAdd(&p.counters[tile], 1u);
-                    *sh_last = (old == (unsigned)p.splits - 1) ? 1 : 0;
-                }
-                asm volatile("bar.sync 2, 128;" ::: "memory");
-                if (*sh_last) {
-                    __threadfence();
-                    const float* base = p.partials + (size_t)tile * p.splits * NT * 128;
-#pragma unroll 4
-                    for (int j = 0; j < NT; ++j) {
-                        float sum = 0.f;
-                        for (int sp = 0; sp < p.splits; ++sp) sum += __ldcg(base + ((size_t)sp * NT + j) * 128 + t);
-                        if (valid && tok0 + j < p.M) p.y[(size_t)(tok0 + j) * p.N + n] = f32_to_bf16_rn(sum);
+                        for (int i = 0; i < kBatch; i += 2)
+                            acc[(c0 + i) / 2] = __ffma2_rn(
+                                sc2, make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), acc[(c0 + i) / 2]);
                     }
-                    if (t == 0) p.counters[tile] = 0u;
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&d_empty[b]);
+                }
+                sr0 = sr1;
+                sr1 = sr2;
+                sr2 = sr3;
+                sr3 = next_scale();
+                if (!ok) *abort_flag = 1;
+            }
+            // ---- end of unit: this warpgroup writes its CW tokens of the tile
+            const bool all_ok = bar_and(4, 128 * R, ok && !*abort_flag);
+            const int n = 128 * ui.nb + t;
+            const int tok0 = ui.mb * NT + r * CW;
+            if (all_ok) {
+                if (p.splits == 1) {
+                    if (t < W) {
+#pragma unroll
+                        for (int j = 0; j < CW; ++j)
+                            if (tok0 + j < p.M)
+                                p.y[(size_t)(tok0 + j) * p.N + n] =
+                                    f32_to_bf16_rn((j & 1) ? acc[j / 2].y : acc[j / 2].x);
+                    }
+                } else {
+                    const int tile = ui.mb * p.NB + ui.nb;
+                    // partial sums: [tile][split][column t][NT tokens], this warpgroup's CW tokens
+                    float4* part = reinterpret_cast<float4*>(p.partials + (((size_t)tile * p.splits + ui.split) * 128 + t) * NT + r * CW);
+#pragma unroll
+                    for (int j = 0; j < CW; j += 4)
+                        part[j / 4] = make_float4(acc[j / 2].x, acc[j / 2].y, acc[j / 2 + 1].x, acc[j / 2 + 1].y);
+                    __threadfence();
+                    asm volatile("bar.sync 5, %0;" ::"r"(128 * R) : "memory");
+                    if (rt == 0) {
+                        const unsigned old = atomicAdd(&p.counters[tile], 1u);
+                        *sh_last = (old == (unsigned)p.splits - 1) ? 1 : 0;
+                    }
+                    asm volatile("bar.sync 5, %0;" ::"r"(128 * R) : "memory");
+                    if (*sh_last) {
+                        __threadfence();
+                        // every split's values for this thread, summed in split order,
+                        // 16 tokens at a time
+                        const float4* base = reinterpret_cast<const float4*>(p.partials + ((size_t)tile * p.splits * 128 + t) * NT + r * CW);
+                        const size_t sstride = (size_t)128 * NT / 4;  // float4s between splits
+#pragma unroll 1
+                        for (int j0 = 0; j0 < CW; j0 += 16) {
+                            float4 sum[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) sum[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                            for (int sp = 0; sp < p.splits; ++sp) {
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const float4 v = __ldcg(base + sp * sstride + j0 / 4 + j);
+                                    sum[j].x += v.x;
+                                    sum[j].y += v.y;
+                                    sum[j].z += v.z;
+                                    sum[j].w += v.w;
+                                }
+                            }
+                            if (t < W) {
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) {
+                                    const float4& v = sum[j / 4];
+                                    const float val = (j & 3) == 0 ? v.x : (j & 3) == 1 ? v.y : (j & 3) == 2 ? v.z : v.w;
+                                    if (j0 + j < CW && tok0 + j0 + j < p.M)
+                                        p.y[(size_t)(tok0 + j0 + j) * p.N + n] = f32_to_bf16_rn(val);
+                                }
+                            }
+                        }
+                        if (rt == 0) p.counters[tile] = 0u;
+                    }
+                    asm volatile("bar.sync 5, %0;" ::"r"(128 * R) : "memory");  // sh_last is reused
                 }
             }
+#pragma unroll
+            for (int j = 0; j < CW / 2; ++j) acc[j] = make_float2(0.f, 0.f);
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == C::kProdWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, S::kTmemCols);
+        tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-
-
-static int tc_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+static int tc_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 128; }
 
 bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
     const Layout L(K, N);
     const int G = K / 128;
     const int NT = tc_nt(M);
     const int MT = (M + NT - 1) / NT;
+    const long long slots = sms;  // one CTA per SM
     const long long tiles = (long long)L.NB * MT;
-    // split K so that the grid covers the SMs about once (at least 2 groups a split)
+    // split K when there are fewer tiles than SMs (at least 2 groups a split)
     int splits = 1;
-    if (tiles < sms) {
-        splits = (int)((sms + tiles - 1) / tiles);
+    if (tiles < slots) {
+        splits = (int)((slots + tiles - 1) / tiles);
         const int max_split = G / 2 > 0 ? G / 2 : 1;
         if (splits > max_split) splits = max_split;
     }
     if (splits > 1 && (size_t)tiles > kMaxCounters) splits = 1;
+    const long long units = tiles * splits;
+    if (units >= (1ll << 31)) return false;
     out->NT = NT;
     out->MT = MT;
     out->NB = L.NB;
     out->splits = splits;
-    switch (NT) {
-        case 16: out->smem = TcSmem<16>::kAlloc; break;
-        case 32: out->smem = TcSmem<32>::kAlloc; break;
-        case 64: out->smem = TcSmem<64>::kAlloc; break;
-        default: out->smem = TcSmem<128>::kAlloc; break;
-    }
+    out->ctas = (int)(units < slots ? units : slots);
+    out->smem = NT == 16 ? TcCfg<16>::kAlloc : NT == 32 ? TcCfg<32>::kAlloc : TcCfg<128>::kAlloc;
     out->ws_bytes = splits > 1 ? ws_counter_bytes(tiles) + (size_t)tiles * splits * NT * 128 * sizeof(float) : 0;
     return true;
 }
@@ -396,12 +534,11 @@ static cudaError_t launch_nt(const CUtensorMap& tm, const TcParams& prm, const T
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!set_for[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcSmem<NT>::kAlloc);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<NT>::kAlloc);
         if (e != cudaSuccess) return e;
         set_for[dev] = 1;
     }
-    dim3 grid(plan.NB, plan.MT, plan.splits);
-    return launch_kernel(kern, grid, dim3(kThreads), plan.smem, s, pdl, tm, prm);
+    return launch_kernel(kern, dim3(plan.ctas), dim3(TcCfg<NT>::kThreads), plan.smem, s, pdl, tm, prm);
 }
 
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
@@ -410,15 +547,16 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
     auto encode = get_encode();
     if (!encode) return cudaErrorNotSupported;
     CUtensorMap tm;
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)plan.NT};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+    // x viewed as [K/64 slabs][M tokens][64 columns]: one box is NT tokens x
+    // two slabs of 64 columns, i.e. one group of 128 rows of K
+    const cuuint64_t dims[3] = {64, (cuuint64_t)M, (cuuint64_t)(K / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)K * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)plan.NT, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(x), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    const Layout L(K, N);
     TcParams prm;
     prm.qd = qd;
     prm.scales = scales;
@@ -434,12 +572,12 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
     prm.NB = plan.NB;
     prm.MT = plan.MT;
     prm.splits = plan.splits;
+    prm.units = plan.NB * plan.MT * plan.splits;
     const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     switch (plan.NT) {
         case 16: return launch_nt<16>(tm, prm, plan, s, pdl);
         case 32: return launch_nt<32>(tm, prm, plan, s, pdl);
-        case 64: return launch_nt<64>(tm, prm, plan, s, pdl);
         default: return launch_nt<128>(tm, prm, plan, s, pdl);
     }
 }

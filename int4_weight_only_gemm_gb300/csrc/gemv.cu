@@ -41,17 +41,20 @@ struct GemvParams {
     float* partials;
     int M, N, K, KB, NB;
     int cpt;        // chunks per tile = 4 * KB
-    long long C;    // total chunks
+    int C;          // total chunks
     int P;          // workers
+    int q, r;       // C = q * P + r: worker w takes q chunks, plus one if w < r
     int prefetch;   // weights may be loaded before the preceding grid completes
 };
 
 constexpr int kGemvWG = 4;  // worker warpgroups per CTA
 constexpr int kGemvMaxSmem = 200 * 1024;  // activation copy + chunk sums
 
-__device__ __forceinline__ long long worker_begin(long long w, long long C, int P) { return w * C / P; }
-__device__ __forceinline__ int worker_of(long long c, long long C, int P) {
-    return (int)(((c + 1) * (long long)P - 1) / C);
+// Division-free equal split of the C chunks over P workers.
+__device__ __forceinline__ int worker_begin(int w, const GemvParams& p) { return w * p.q + (w < p.r ? w : p.r); }
+__device__ __forceinline__ int worker_of(int c, const GemvParams& p) {
+    const int big = p.r * (p.q + 1);
+    return c < big ? c / (p.q + 1) : p.r + (c - big) / p.q;
 }
 
 __device__ __forceinline__ uint4 ld_stream_v4(const uint32_t* p) {
@@ -66,14 +69,23 @@ __device__ __forceinline__ void wg_bar(int wg) {
     asm volatile("bar.sync %0, 128;" ::"r"(wg + 1) : "memory");
 }
 
+// One chunk's data for one thread: its column's 4 words (32 rows), the
+// group's scale (binary16 bits) and the word holding its zero point.
+struct ChunkData {
+    uint4 w;
+    uint32_t s, zw;
+};
+
+// Write a finished tile segment: directly when this worker owns the whole
+// tile, else as a partial sum with the ordered last-arrival reduction.
 template <int M>
-__device__ __forceinline__ void gemv_flush(const GemvParams& p, int worker, int wg, int t, int nb, long long a,
-                                           long long b, long long my_begin, float (&acc)[M], int* sh_last) {
+__device__ __forceinline__ void gemv_flush(const GemvParams& p, int worker, int wg, int t, int nb, int a, int b,
+                                           int my_begin, const float (&acc)[M], int* sh_last) {
     const Layout L(p.K, p.N);
     const int W = L.width(nb);
     const int n = 128 * nb + t;
-    const long long t0 = (long long)nb * p.cpt, t1 = t0 + p.cpt;
-    if (a == t0 && b == t1) {  // whole tile owned: write y directly
+    const int t0 = nb * p.cpt, t1 = t0 + p.cpt;
+    if (a == t0 && b == t1) {
         if (t < W) {
 #pragma unroll
             for (int m = 0; m < M; ++m)
@@ -81,27 +93,25 @@ __device__ __forceinline__ void gemv_flush(const GemvParams& p, int worker, int 
         }
         return;
     }
-    const int slot = (my_begin / p.cpt == nb) ? 0 : 1;
+    const int slot = (my_begin >= t0) ? 0 : 1;  // first tile of this worker, or its last
     float* part = p.partials + ((size_t)(worker * 2 + slot) * M) * 128;
 #pragma unroll
     for (int m = 0; m < M; ++m) part[m * 128 + t] = acc[m];
     __threadfence();
     wg_bar(wg);
+    const int wf = worker_of(t0, p), wl = worker_of(t1 - 1, p);
     if (t == 0) {
-        const int wf = worker_of(t0, p.C, p.P), wl = worker_of(t1 - 1, p.C, p.P);
-        const unsigned target = (unsigned)(wl - wf + 1);
         const unsigned old = atomicAdd(&p.counters[nb], 1u);
-        sh_last[wg] = (old == target - 1) ? 1 : 0;
+        sh_last[wg] = (old == (unsigned)(wl - wf)) ? 1 : 0;
     }
     wg_bar(wg);
     if (sh_last[wg]) {
         __threadfence();
-        const int wf = worker_of(t0, p.C, p.P), wl = worker_of(t1 - 1, p.C, p.P);
         float sum[M];
 #pragma unroll
         for (int m = 0; m < M; ++m) sum[m] = 0.f;
-        for (int w = wf; w <= wl; ++w) {
-            const int s = (worker_begin(w, p.C, p.P) / p.cpt == nb) ? 0 : 1;
+        for (int w = wf; w <= wl; ++w) {  // fixed order: deterministic
+            const int s = (worker_begin(w, p) >= t0) ? 0 : 1;
             const float* q = p.partials + ((size_t)(w * 2 + s) * M) * 128;
 #pragma unroll
             for (int m = 0; m < M; ++m) sum[m] += __ldcg(q + m * 128 + t);
@@ -127,34 +137,80 @@ __global__ void __launch_bounds__(128 * kGemvWG, 1) gemv_kernel(const GemvParams
     const int t = tid & 127;
     const int worker = blockIdx.x * kGemvWG + wg;
     const Layout L(p.K, p.N);
-    const long long c_begin = worker < p.P ? worker_begin(worker, p.C, p.P) : 0;
-    const long long c_end = worker < p.P ? worker_begin(worker + 1, p.C, p.P) : 0;
+    const bool active = worker < p.P;
+    const int c_begin = active ? worker_begin(worker, p) : 0;
+    const int c_end = active ? worker_begin(worker + 1, p) : 0;
 
-    // 1. first weight loads go out before anything else
-    uint4 buf[D];
-    auto load_chunk = [&](long long c) -> uint4 {
-        const int nb = (int)(c / p.cpt);
-        const int rem = (int)(c - (long long)nb * p.cpt);
-        const int W = L.width(nb);
-        if (t >= W) return make_uint4(0, 0, 0, 0);
-        const uint32_t* src = p.qd + L.block_word(nb, rem >> 2) + ((size_t)(rem & 3) * W + t) * 4;
-        return ld_stream_v4(src);
+    // Load cursor: chunks are fetched in increasing order, D ahead of use,
+    // through pointers that advance by constant steps.  In full tiles chunk
+    // c sits at word 512 c; in the ragged last tile chunks are W*4 words.
+    // Threads beyond a ragged tile's width read column W-1 (a valid address)
+    // and discard the result, so the loop has no per-thread branches.
+    int l_nb = c_begin / (p.cpt > 0 ? p.cpt : 1);
+    int l_rem = c_begin - l_nb * p.cpt;
+    int l_left = c_end - c_begin;
+    const uint32_t* wp;
+    const uint16_t* sp;
+    const uint32_t* zp;
+    int wstep;
+    auto seek_tile = [&]() {  // pointers for chunk (l_nb, l_rem)
+        const int W = L.width(l_nb);
+        const int tc = t < W ? t : W - 1;
+        const int kb = l_rem >> 2;
+        wstep = W * 4;  // one chunk: W columns x 4 words
+        wp = p.qd + L.block_word(l_nb, kb) + ((size_t)(l_rem & 3) * W + tc) * 4;
+        const int n = 128 * l_nb + tc;
+        sp = p.scales + (size_t)kb * p.N + n;
+        zp = p.qzeros + (size_t)kb * (p.N / 8) + (n >> 3);
     };
+    if (l_left > 0) seek_tile();
+    else {
+        wp = p.qd;
+        sp = p.scales;
+        zp = p.qzeros;
+        wstep = 0;
+    }
+    auto next_chunk = [&]() -> ChunkData {
+        ChunkData d;
+        d.w = ld_stream_v4(wp);
+        d.s = __ldg(sp);
+        d.zw = __ldg(zp);
+        if (l_left > 1) {
+            --l_left;
+            ++l_rem;
+            if (l_rem == p.cpt) {  // next tile (rare, uniform across the warpgroup)
+                l_rem = 0;
+                ++l_nb;
+                seek_tile();
+            } else {
+                wp += wstep;
+                if ((l_rem & 3) == 0) {  // next group of 128 rows
+                    sp += p.N;
+                    zp += p.N / 8;
+                }
+            }
+        } else {
+            l_left = 0;  // stay on the last chunk: later loads re-read it and are never used
+        }
+        return d;
+    };
+
     // With static weights the first loads go out before waiting on the
     // preceding grid; otherwise after it (x, y and the workspace are always
     // touched only after the wait).
+    ChunkData buf[D];
     if (p.prefetch) {
 #pragma unroll
-        for (int i = 0; i < D; ++i) buf[i] = (c_begin + i < c_end) ? load_chunk(c_begin + i) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < D; ++i) buf[i] = next_chunk();
     }
     pdl_wait();
     if (!p.prefetch) {
 #pragma unroll
-        for (int i = 0; i < D; ++i) buf[i] = (c_begin + i < c_end) ? load_chunk(c_begin + i) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < D; ++i) buf[i] = next_chunk();
     }
     pdl_launch_dependents();  // one wave: the next grid can only start where this one ends
 
-    // 2. activations to shared memory, then per-chunk sums
+    // activations to shared memory, then per-32-row chunk sums
     {
         const int nvec = p.M * p.K / 8;  // 16-byte vectors of x actually present
         const uint4* xg = reinterpret_cast<const uint4*>(p.x);
@@ -175,69 +231,68 @@ __global__ void __launch_bounds__(128 * kGemvWG, 1) gemv_kernel(const GemvParams
         }
         __syncthreads();
     }
-    if (worker >= p.P) return;  // no named barrier is shared across warpgroups
+    if (!active) return;  // no named barrier is shared across warpgroups
 
-    float acc[M];
+    // Tile segments: [seg_a, seg_b) lies in one tile.  Buffer slot i holds
+    // chunk c with (c - c_begin) % D == i, so segments walk the same D-groups.
+    int seg_a = c_begin;
+    int group_base = c_begin;
+    while (seg_a < c_end) {
+        const int nb = seg_a / p.cpt;
+        const int tile_end = (nb + 1) * p.cpt;
+        const int seg_b = c_end < tile_end ? c_end : tile_end;
+        const int n = 128 * nb + t;
+        const int zshift = 4 * (n & 7);
+        float acc[M];
 #pragma unroll
-    for (int m = 0; m < M; ++m) acc[m] = 0.f;
-    int cur_nb = (int)(c_begin / p.cpt);
-    long long seg_first = c_begin;
-
-    for (long long c0 = c_begin; c0 < c_end; c0 += D) {
+        for (int m = 0; m < M; ++m) acc[m] = 0.f;
+        for (int base = group_base; base < seg_b; base += D) {
 #pragma unroll
-        for (int i = 0; i < D; ++i) {
-            const long long c = c0 + i;
-            if (c < c_end) {
-                const uint4 cur = buf[i];
-                if (c + D < c_end) buf[i] = load_chunk(c + D);
-                const int nb = (int)(c / p.cpt);
-                if (nb != cur_nb) {
-                    gemv_flush<M>(p, worker, wg, t, cur_nb, seg_first, c, c_begin, acc, sh_last);
+            for (int i = 0; i < D; ++i) {
+                const int c = base + i;
+                if (c >= seg_a && c < seg_b) {
+                    const ChunkData cur = buf[i];
+                    buf[i] = next_chunk();
+                    {
+                        const int rem = c - nb * p.cpt;
+                        const int k0 = (rem >> 2) * 128 + (rem & 3) * 32;
+                        const float s = f16_bits_to_f32((uint16_t)cur.s);
+                        const float zoff = 128.f + (float)((cur.zw >> zshift) & 0xFu);
+                        // four independent accumulation chains per token (one per word)
+                        float d[4][M];
+                        const uint32_t wv[4] = {cur.w.x, cur.w.y, cur.w.z, cur.w.w};
 #pragma unroll
-                    for (int m = 0; m < M; ++m) acc[m] = 0.f;
-                    cur_nb = nb;
-                    seg_first = c;
-                }
-                const int rem = (int)(c - (long long)nb * p.cpt);
-                const int kb = rem >> 2;
-                const int k0 = kb * 128 + (rem & 3) * 32;
-                const int n = 128 * nb + t;
-                if (t < L.width(nb)) {
-                    const float s = f16_bits_to_f32(__ldg(p.scales + (size_t)kb * p.N + n));
-                    const uint32_t zw = __ldg(p.qzeros + (size_t)kb * (p.N / 8) + (n >> 3));
-                    const float zoff = 128.f + (float)((zw >> (4 * (n & 7))) & 0xFu);
-                    // four independent accumulation chains per token (one per word)
-                    float d[4][M];
-                    const uint32_t wv[4] = {cur.x, cur.y, cur.z, cur.w};
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t wp[4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t wp[4];
+                            for (int qq = 0; qq < 4; ++qq) wp[qq] = magic_pair(wv[j], qq);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) wp[q] = magic_pair(wv[j], q);
+                            for (int m = 0; m < M; ++m) {
+                                const uint4 xq = *reinterpret_cast<const uint4*>(xs + (size_t)m * p.K + k0 + 8 * j);
+                                const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
+                                float a = 0.f;
+#pragma unroll
+                                for (int qq = 0; qq < 4; ++qq) {
+                                    a = fma_lo(wp[qq], xp[qq], a);
+                                    a = fma_hi(wp[qq], xp[qq], a);
+                                }
+                                d[j][m] = a;
+                            }
+                        }
+                        const int kc = k0 >> 5;
 #pragma unroll
                         for (int m = 0; m < M; ++m) {
-                            const uint4 xq = *reinterpret_cast<const uint4*>(xs + (size_t)m * p.K + k0 + 8 * j);
-                            const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
-                            float a = 0.f;
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                a = fma_lo(wp[q], xp[q], a);
-                                a = fma_hi(wp[q], xp[q], a);
-                            }
-                            d[j][m] = a;
+                            const float dot = (d[0][m] + d[1][m]) + (d[2][m] + d[3][m]);
+                            acc[m] = fmaf(s, fmaf(-zoff, xsum[m * (p.K / 32) + kc], dot), acc[m]);
                         }
-                    }
-                    const int kc = k0 >> 5;
-#pragma unroll
-                    for (int m = 0; m < M; ++m) {
-                        const float dot = (d[0][m] + d[1][m]) + (d[2][m] + d[3][m]);
-                        acc[m] = fmaf(s, fmaf(-zoff, xsum[m * (p.K / 32) + kc], dot), acc[m]);
                     }
                 }
             }
         }
+        gemv_flush<M>(p, worker, wg, t, nb, seg_a, seg_b, c_begin, acc, sh_last);
+        group_base = seg_b - (seg_b - c_begin) % D;
+        seg_a = seg_b;
     }
-    gemv_flush<M>(p, worker, wg, t, cur_nb, seg_first, c_end, c_begin, acc, sh_last);
 }
 
 // ---------------------------------------------------------------------------
@@ -252,6 +307,7 @@ bool gemv_plan(int M, int N, int K, int sms, GemvPlan* out) {
     const int MT = gemv_mtile(M);
     const Layout L(K, N);
     const long long C = (long long)L.NB * 4 * L.KB;
+    if (C >= (1ll << 31)) return false;
     const size_t smem = (size_t)MT * K * 2 + (size_t)MT * (K / 32) * 4;
     if (smem > (size_t)kGemvMaxSmem) return false;
     if ((size_t)L.NB > kMaxCounters) return false;
@@ -268,7 +324,7 @@ bool gemv_plan(int M, int N, int K, int sms, GemvPlan* out) {
 
 template <int M>
 static cudaError_t launch_m(const GemvParams& prm, const GemvPlan& plan, cudaStream_t s, bool pdl) {
-    constexpr int D = 4;
+    constexpr int D = M == 1 ? 8 : M == 2 ? 6 : M == 4 ? 4 : 2;  // chunks in flight per thread
     auto kern = gemv_kernel<M, D>;
     // the dynamic shared memory limit is raised once per device to the maximum
     // any plan asks for, so that launches (also inside graph capture) make no
@@ -304,8 +360,10 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qd, const uint16_t* s
     prm.KB = L.KB;
     prm.NB = L.NB;
     prm.cpt = 4 * L.KB;
-    prm.C = plan.C;
+    prm.C = (int)plan.C;
     prm.P = plan.P;
+    prm.q = (int)(plan.C / plan.P);
+    prm.r = (int)(plan.C % plan.P);
     const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     switch (gemv_mtile(M)) {

@@ -27,6 +27,7 @@ int gemv_read_status();
 // tcgen05 tensor-core GEMM (any M)
 struct TcPlan {
     int NT, MT, NB, splits;  // tokens per tile, token tiles, column tiles, K splits
+    int ctas;                // persistent CTAs
     size_t smem, ws_bytes;
 };
 bool tc_plan(int M, int N, int K, int sms, TcPlan* out);
