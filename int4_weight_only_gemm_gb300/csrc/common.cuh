@@ -103,11 +103,13 @@ W4A16_DEVICE bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
 
 // Bounded wait for the phase with the given parity to complete.  `abort` is a
 // shared flag: once any thread of the CTA has given up, the others stop
-// waiting at once.  The clock is read only every 1024 polls, so a wait that
-// succeeds soon costs nothing but the polls.  Returns false on timeout or abort.
+// waiting at once.  A phase that has already completed costs one poll: the
+// flag is read only after a failed poll, and the clock only every 1024 polls.
+// Returns false on timeout or abort.
 W4A16_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
                             uint64_t limit_ns = kWaitNs) {
     const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
     if (abort && *abort) return false;
     uint64_t t0 = 0;
     for (uint32_t i = 0; i < kWaitSpins; ++i) {
@@ -197,6 +199,13 @@ W4A16_DEVICE void tma_load_2d(void* smem_dst, const void* tmap, int x, int y, ui
 // 4-byte asynchronous copy global -> shared (completion tracked below)
 W4A16_DEVICE void cp_async_4(void* smem_dst, const void* gsrc) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+// Close the group of this thread's cp.async copies issued since the last commit.
+W4A16_DEVICE void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+W4A16_DEVICE void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 // The mbarrier's current phase also waits for this thread's earlier cp.async
 // copies (net-zero change to the arrival count).

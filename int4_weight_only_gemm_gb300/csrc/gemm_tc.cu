@@ -74,7 +74,9 @@ struct TcCfg {
     static constexpr int kXOff = 0;
     static constexpr int kPOff = kXOff + SS * kXStage;   // packed weights, 8 KB per stage
     static constexpr int kZOff = kPOff + SS * 8192;      // zero words, 64 bytes per stage
-    static constexpr int kBarOff = kZOff + SS * 64;
+    static constexpr int kSP = 6;                        // scale words each rescale thread loads ahead
+    static constexpr int kSclOff = kZOff + SS * 64;      // [kSP][128 * R] scale words (two fp16 columns each)
+    static constexpr int kBarOff = kSclOff + kSP * 128 * R * 4;
     static constexpr int kBytes = kBarOff + 1024;
     static constexpr int kAlloc = kBytes + 1024;         // slack for the alignment
     // tensor memory: SA A-buffers of 64 columns, then the D ring of NDB x NT columns
@@ -287,50 +289,43 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issue
-        // The one warp of the CTA that issues tcgen05.mma (an elected lane).
-        // It needs only the flat group index q, and takes two groups a pass
-        // (their waits, then their 16 MMAs), halving its per-group overhead.
+        // The one thread of the CTA that issues tcgen05.mma: the whole loop runs
+        // in an elected lane, so a barrier that has already completed costs a
+        // single poll and no warp vote.  It needs only the flat group index q.
         constexpr uint32_t idesc = idesc_bf16_f32(128, NT);
         int Q = 0;  // groups this CTA processes
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const UnitInfo ui = unit_info(p, u);
             Q += ui.g1 - ui.g0;
         }
-        bool ok = true;
-        for (int q0 = 0; q0 < Q; q0 += 2) {
-            const int nq = Q - q0 < 2 ? Q - q0 : 2;
-            for (int i = 0; i < nq; ++i) {
-                const int q = q0 + i;
-                if (ok && !mbar_wait_warp(&a_full[q % SA], (q / SA) & 1, abort_flag, &g_tc_status)) ok = false;
+        if (elect_one()) {
+            bool ok = true;
+            for (int q = 0; q < Q; ++q) {
+                if (!mbar_wait(&a_full[q % SA], (q / SA) & 1, abort_flag, &g_tc_status)) ok = false;
                 // D buffer q % NDB is free once every rescale warp has read group q - NDB
                 if (ok && q >= C::NDB &&
-                    !mbar_wait_warp(&d_empty[q % C::NDB], ((q / C::NDB) - 1) & 1, abort_flag, &g_tc_status))
+                    !mbar_wait(&d_empty[q % C::NDB], ((q / C::NDB) - 1) & 1, abort_flag, &g_tc_status))
                     ok = false;
-            }
-            if (ok) {
-                tc_fence_after();
-                if (elect_one()) {
-                    for (int i = 0; i < nq; ++i) {
-                        const int q = q0 + i;
-                        const uint32_t xaddr = smem_u32(smem + C::kXOff + (q % SS) * C::kXStage);
-                        const uint32_t a_tmem = tmem + C::kTmemA + (q % SA) * 64;
-                        const uint32_t d_tmem = tmem + C::kTmemD + (q % C::NDB) * NT;
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t bdesc = smem_desc_sw128(xaddr + (kk >> 2) * (NT * 128) + (kk & 3) * 32);
-                            mma_bf16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&done[q % ND]);
-                    }
+                if (!ok) {
+                    *abort_flag = 1;
+                    break;
                 }
-                __syncwarp();
+                tc_fence_after();
+                const uint32_t xaddr = smem_u32(smem + C::kXOff + (q % SS) * C::kXStage);
+                const uint32_t a_tmem = tmem + C::kTmemA + (q % SA) * 64;
+                const uint32_t d_tmem = tmem + C::kTmemD + (q % C::NDB) * NT;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t bdesc = smem_desc_sw128(xaddr + (kk >> 2) * (NT * 128) + (kk & 3) * 32);
+                    mma_bf16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&done[q % ND]);
             }
-            if (!ok) *abort_flag = 1;
+            // every MMA issued must be complete before TMEM is freed
+            mma_commit(mma_done);
         }
-        pdl_launch_dependents();  // this CTA issues no more tensor work
-        // every MMA issued must be complete before TMEM is freed
-        if (elect_one()) mma_commit(mma_done);
         __syncwarp();
+        pdl_launch_dependents();  // this CTA issues no more tensor work
         (void)mbar_wait(mma_done, 0, nullptr, &g_tc_status);
     } else {
         // ------------------------------------------------------- rescale + epilogue
@@ -344,39 +339,48 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
         float2 acc[CW / 2];
 #pragma unroll
         for (int j = 0; j < CW / 2; ++j) acc[j] = make_float2(0.f, 0.f);
-        // scales of this thread's column for the next groups, loaded ahead of use
+        // Scales of this thread's column, kSP groups ahead: a private ring of
+        // 4-byte words (the column's fp16 scale and its neighbour's) filled by
+        // cp.async, one commit group per group of K, so that waiting for group
+        // q's word never waits for the loads issued after it.
+        uint32_t* const sring = reinterpret_cast<uint32_t*>(smem + C::kSclOff) + rt;
         int lq_u = blockIdx.x, lq_g = -1;  // load cursor over (unit, group)
         int lq_nb = 0, lq_g1 = 0;
-        auto next_scale = [&]() -> float {
-            if (lq_u >= p.units) return 0.f;
-            if (lq_g < 0 || lq_g >= lq_g1) {  // first call or past the unit's last group
-                if (lq_g >= 0) {
-                    lq_u += gridDim.x;
-                    if (lq_u >= p.units) return 0.f;
+        auto issue_scale = [&](int slot) {
+            if (lq_u < p.units && (lq_g < 0 || lq_g >= lq_g1)) {  // first call or past the unit's last group
+                if (lq_g >= 0) lq_u += gridDim.x;
+                if (lq_u < p.units) {
+                    const UnitInfo ui = unit_info(p, lq_u);
+                    lq_nb = ui.nb;
+                    lq_g = ui.g0;
+                    lq_g1 = ui.g1;
                 }
-                const UnitInfo ui = unit_info(p, lq_u);
-                lq_nb = ui.nb;
-                lq_g = ui.g0;
-                lq_g1 = ui.g1;
             }
-            const int W = L.width(lq_nb);
-            const int tc = t < W ? t : W - 1;
-            const float v = f16_bits_to_f32(__ldg(p.scales + (size_t)lq_g * p.N + 128 * lq_nb + tc));
-            ++lq_g;
-            return v;
+            if (lq_u < p.units) {
+                const int W = L.width(lq_nb);
+                const int tc = (t < W ? t : W - 1) & ~1;
+                cp_async_4(sring + slot * 128 * R, p.scales + (size_t)lq_g * p.N + 128 * lq_nb + tc);
+                ++lq_g;
+            }
+            cp_async_commit();  // possibly empty: keeps one group per slot
         };
-        float sr0 = next_scale(), sr1 = next_scale(), sr2 = next_scale(), sr3 = next_scale();
+#pragma unroll 1
+        for (int i = 0; i < C::kSP; ++i) issue_scale(i);
         int q = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const UnitInfo ui = unit_info(p, u);
             const int W = L.width(ui.nb);
+            const int odd = (t < W ? t : W - 1) & 1;  // which half of the scale word is this column's
             for (int g = ui.g0; g < ui.g1; ++g, ++q) {
                 const int b = q % C::NDB;
+                cp_async_wait<C::kSP - 1>();  // group q's scale word has landed
+                const uint32_t sw = lds_u32(smem_u32(sring + (q % C::kSP) * 128 * R));
+                const float sc = f16_bits_to_f32((unsigned short)(odd ? sw >> 16 : sw & 0xFFFFu));
                 if (ok && !mbar_wait_warp(&done[q % ND], (q / ND) & 1, abort_flag, &g_tc_status)) ok = false;
                 if (ok) {
                     tc_fence_after();
-                    const float2 sc2 = make_float2(sr0, sr0);
+                    const float2 sc2 = make_float2(sc, sc);
                     const uint32_t dbase = tmem + lane_base + C::kTmemD + b * NT + r * CW;
 #pragma unroll
                     for (int c0 = 0; c0 < CW; c0 += kBatch) {
@@ -394,10 +398,8 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&d_empty[b]);
                 }
-                sr0 = sr1;
-                sr1 = sr2;
-                sr2 = sr3;
-                sr3 = next_scale();
+                // the slot just read is refilled only after sc was consumed above
+                issue_scale(q % C::kSP);
                 if (!ok) *abort_flag = 1;
             }
             // ---- end of unit: this warpgroup writes its CW tokens of the tile
@@ -467,6 +469,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < CW / 2; ++j) acc[j] = make_float2(0.f, 0.f);
         }
+        cp_async_wait<0>();  // the trailing commit groups are empty; nothing stays in flight
     }
 
     tc_fence_before();
@@ -489,10 +492,12 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
     const int MT = (M + NT - 1) / NT;
     const long long slots = sms;  // one CTA per SM
     const long long tiles = (long long)L.NB * MT;
-    // split K when there are fewer tiles than SMs (at least 2 groups a split)
+    // Split K when there are fewer tiles than SMs (at least 2 groups a split),
+    // rounding down: every CTA then runs at most one unit, so no SM does twice
+    // the work of the others while most idle.
     int splits = 1;
     if (tiles < slots) {
-        splits = (int)((slots + tiles - 1) / tiles);
+        splits = (int)(slots / tiles);
         const int max_split = G / 2 > 0 ? G / 2 : 1;
         if (splits > max_split) splits = max_split;
     }
