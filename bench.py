@@ -341,6 +341,29 @@ def cpu_baseline(min_seconds=8.0):
             "sample": f"the full decode set (4 projections, M=1) repeated {n} times, {dt:.1f} s"}
 
 
+def run_case(case, reps):
+    """One seeded GEMM of the named layer shape, launched `reps` times back to
+    back on the current stream (the workload of the ncu summaries)."""
+    import torch
+    import int4_weight_only_gemm_gb300 as w
+    parts = case.split(":")
+    shape, M = parts[0], int(parts[1])
+    path = int(parts[2]) if len(parts) > 2 else 0
+    p = wi.generate_named(shape, M, 1)
+    x, qw, sc, qz = w.to_device(p)
+    qd = w.w4a16_pack(qw)
+    del qw
+    y = torch.empty((M, p.N), dtype=torch.bfloat16, device="cuda")
+    ws = w.new_workspace(w.w4a16_workspace_bytes(M, p.N, p.K, path=path), "cuda")
+    for _ in range(reps):
+        w.w4a16_gemm(x, qd, sc, qz, path=path, workspace=ws, out=y)
+    torch.cuda.synchronize()
+    st = w.w4a16_last_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {w.w4a16_status_str(st)}")
+    print(json.dumps({"case": case, "reps": reps, "path": path, "ok": True}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -350,7 +373,14 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the M=16 / M=2048 / per-GEMM extras")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer measurement")
+    ap.add_argument("--case", default="",
+                    help="SHAPE:M[:PATH] -- run that one GEMM --reps times and exit (for profilers); "
+                         "PATH 0 = auto, 1 = split-K GEMV, 2 = tensor-core kernel")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
+    if args.case:
+        run_case(args.case, args.reps)
+        return
     if args.warmup < 3:
         args.warmup = 3
 
