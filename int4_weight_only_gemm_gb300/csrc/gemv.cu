@@ -6,24 +6,31 @@
 // referee report summary; group size 128 from "Assumptions & free
 // parameters").
 //
-// Work split (stream-K): the packed weights are a sequence of C chunks of
-// 32 rows x one 128-column tile (2 KB, contiguous in the device layout, in
-// (tile, K) order).  P workers (128-thread warpgroups, 4 per CTA, one CTA per
-// SM) take contiguous chunk ranges of equal length, so every SM streams the
-// same number of bytes.  Thread t of a worker owns column t of the current
-// tile and reads its 4 words of a chunk with one 128-bit load; a warp's load
-// is 512 contiguous bytes.
+// Work split: a unit is one 128-row group of K of one 128-column tile (8 KB
+// of packed weights, contiguous in the device layout), units in (tile, K)
+// order.  Each CTA (one per SM) takes a contiguous range of equal length, so
+// every SM streams the same number of bytes.
 //
-// Arithmetic per chunk and token: dot = sum_k (128 + q_k) x_k, with the
-// bfloat16 value 128 + q made by one mask-and-or per pair of rows (exact), and
-// bf16 x bf16 -> f32 fused multiply-adds; then the zero point and scale are
-// applied once per chunk in f32: acc += s (dot - (128 + z) sum_k x_k), using a
-// per-chunk activation sum computed once per CTA.  The scale is used at its
-// full binary16 precision.
+// Data movement: a producer warp copies whole units -- packed weights, the
+// group's fp16 scales and zero words -- into a ring of shared-memory stages
+// with bulk asynchronous copies (mbarrier transaction counts), as far ahead
+// as the ring allows, so a CTA has most of its bytes requested at once and
+// the loads never wait on the arithmetic.
 //
-// Partial tiles (a worker range that starts or ends inside a tile) go to the
-// workspace; the last worker to arrive on a tile (per-tile counter) adds the
-// partials in worker order -- deterministic -- and writes y.
+// Arithmetic: four consumer warpgroups; warpgroup h takes rows 32h..32h+31
+// of every unit and thread t column t: one 128-bit shared load gives its 32
+// codes.  Per token, dot = sum_k (128 + q_k) x_k with the bfloat16 value
+// 128 + q made by one mask-and-or per pair of rows (exact) and bf16 x bf16
+// -> f32 fused multiply-adds; then the zero point and scale are applied once
+// per 32 rows in f32: acc += s (dot - (128 + z) sum_k x_k), with the 32-row
+// activation sums computed once per CTA.  The scale is used at its full
+// binary16 precision.
+//
+// Reduction: at the end of each tile segment the four warpgroups' sums are
+// added through shared memory in warpgroup order.  A tile that lies whole in
+// the CTA's range is written directly; a tile shared by several CTAs leaves
+// one partial per CTA in the workspace, and the last CTA to arrive on the
+// tile's counter adds them in CTA order (deterministic) and writes y.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -40,292 +47,291 @@ struct GemvParams {
     uint32_t* counters;
     float* partials;
     int M, N, K, KB, NB;
-    int cpt;        // chunks per tile = 4 * KB
-    int C;          // total chunks
-    int P;          // workers
-    int q, r;       // C = q * P + r: worker w takes q chunks, plus one if w < r
+    int q, r;       // U = NB * KB units = q * gridDim.x + r: CTA b takes q units, plus one if b < r
+    int S;          // ring stages
     int prefetch;   // weights may be loaded before the preceding grid completes
 };
 
-constexpr int kGemvWG = 4;  // worker warpgroups per CTA
-constexpr int kGemvMaxSmem = 200 * 1024;  // activation copy + chunk sums
+constexpr int kGemvConsumerWarps = 16;                       // four warpgroups
+constexpr int kGemvThreads = 32 * (kGemvConsumerWarps + 1);  // plus the producer warp
+constexpr int kStageW = 0;                                   // packed weights, W * 64 bytes
+constexpr int kStageS = 8192;                                // fp16 scales, W * 2 bytes
+constexpr int kStageZ = 8192 + 256;                          // zero words, W / 2 bytes
+constexpr int kGemvStage = 8192 + 256 + 64;
+constexpr int kGemvMaxStages = 32;
+constexpr int kGemvMaxSmem = 226 * 1024;
 
-// Division-free equal split of the C chunks over P workers.
-__device__ __forceinline__ int worker_begin(int w, const GemvParams& p) { return w * p.q + (w < p.r ? w : p.r); }
-__device__ __forceinline__ int worker_of(int c, const GemvParams& p) {
+// Division-free equal split of the units over the CTAs.
+__device__ __forceinline__ int cta_begin(int b, const GemvParams& p) { return b * p.q + (b < p.r ? b : p.r); }
+__device__ __forceinline__ int cta_of(int u, const GemvParams& p) {
     const int big = p.r * (p.q + 1);
-    return c < big ? c / (p.q + 1) : p.r + (c - big) / p.q;
+    return u < big ? u / (p.q + 1) : p.r + (u - big) / p.q;
 }
 
-__device__ __forceinline__ uint4 ld_stream_v4(const uint32_t* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kGemvConsumerWarps) : "memory"); }
+
+W4A16_DEVICE uint32_t lds_u16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
     return v;
 }
 
-__device__ __forceinline__ void wg_bar(int wg) {
-    asm volatile("bar.sync %0, 128;" ::"r"(wg + 1) : "memory");
-}
-
-// One chunk's data for one thread: its column's 4 words (32 rows), the
-// group's scale (binary16 bits) and the word holding its zero point.
-struct ChunkData {
-    uint4 w;
-    uint32_t s, zw;
+// Shared-memory layout (bytes from the dynamic base), identical on both sides.
+struct GemvSmem {
+    size_t xs, xsum, red, bars, total;
+    __host__ __device__ GemvSmem(int M, int K, int S) {
+        xs = (size_t)S * kGemvStage;                 // ring first (16-byte aligned stages)
+        xsum = xs + (size_t)M * K * 2;               // [M][K] bf16 activations
+        red = xsum + (size_t)M * (K / 32) * 4;       // [M][K/32] 32-row activation sums
+        bars = red + (size_t)4 * M * 128 * 4;        // [4][M][128] warpgroup partial sums
+        total = bars + (size_t)2 * S * 8;            // full[S], empty[S]
+    }
 };
 
-// Write a finished tile segment: directly when this worker owns the whole
-// tile, else as a partial sum with the ordered last-arrival reduction.
 template <int M>
-__device__ __forceinline__ void gemv_flush(const GemvParams& p, int worker, int wg, int t, int nb, int a, int b,
-                                           int my_begin, const float (&acc)[M], int* sh_last) {
+__global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int S = p.S;
+    const GemvSmem lay(M, p.K, S);
+    unsigned char* ring = smem;
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem + lay.xs);
+    float* xsum = reinterpret_cast<float*>(smem + lay.xsum);
+    float* red = reinterpret_cast<float*>(smem + lay.red);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
+    uint64_t* empty = full + S;
+    __shared__ int sh_abort, sh_last;
+    volatile int* abort_flag = &sh_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const Layout L(p.K, p.N);
-    const int W = L.width(nb);
-    const int n = 128 * nb + t;
-    const int t0 = nb * p.cpt, t1 = t0 + p.cpt;
-    if (a == t0 && b == t1) {
-        if (t < W) {
-#pragma unroll
-            for (int m = 0; m < M; ++m)
-                if (m < p.M) p.y[(size_t)m * p.N + n] = f32_to_bf16_rn(acc[m]);
-        }
-        return;
-    }
-    const int slot = (my_begin >= t0) ? 0 : 1;  // first tile of this worker, or its last
-    float* part = p.partials + ((size_t)(worker * 2 + slot) * M) * 128;
-#pragma unroll
-    for (int m = 0; m < M; ++m) part[m * 128 + t] = acc[m];
-    __threadfence();
-    wg_bar(wg);
-    const int wf = worker_of(t0, p), wl = worker_of(t1 - 1, p);
-    if (t == 0) {
-        const unsigned old = atomicAdd(&p.counters[nb], 1u);
-        sh_last[wg] = (old == (unsigned)(wl - wf)) ? 1 : 0;
-    }
-    wg_bar(wg);
-    if (sh_last[wg]) {
-        __threadfence();
-        float sum[M];
-#pragma unroll
-        for (int m = 0; m < M; ++m) sum[m] = 0.f;
-        for (int w = wf; w <= wl; ++w) {  // fixed order: deterministic
-            const int s = (worker_begin(w, p) >= t0) ? 0 : 1;
-            const float* q = p.partials + ((size_t)(w * 2 + s) * M) * 128;
-#pragma unroll
-            for (int m = 0; m < M; ++m) sum[m] += __ldcg(q + m * 128 + t);
-        }
-        if (t < W) {
-#pragma unroll
-            for (int m = 0; m < M; ++m)
-                if (m < p.M) p.y[(size_t)m * p.N + n] = f32_to_bf16_rn(sum[m]);
-        }
-        if (t == 0) p.counters[nb] = 0u;
-    }
-}
+    const int ub = cta_begin(blockIdx.x, p);
+    const int ue = cta_begin(blockIdx.x + 1, p);
 
-template <int M, int D>
-__global__ void __launch_bounds__(128 * kGemvWG, 1) gemv_kernel(const GemvParams p) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                           // [M][K] bf16
-    float* xsum = reinterpret_cast<float*>(smem + (size_t)M * p.K * 2);         // [M][K/32]
-    __shared__ int sh_last[kGemvWG];
-
-    const int tid = threadIdx.x;
-    const int wg = tid >> 7;
-    const int t = tid & 127;
-    const int worker = blockIdx.x * kGemvWG + wg;
-    const Layout L(p.K, p.N);
-    const bool active = worker < p.P;
-    const int c_begin = active ? worker_begin(worker, p) : 0;
-    const int c_end = active ? worker_begin(worker + 1, p) : 0;
-
-    // Load cursor: chunks are fetched in increasing order, D ahead of use,
-    // through pointers that advance by constant steps.  In full tiles chunk
-    // c sits at word 512 c; in the ragged last tile chunks are W*4 words.
-    // Threads beyond a ragged tile's width read column W-1 (a valid address)
-    // and discard the result, so the loop has no per-thread branches.
-    int l_nb = c_begin / (p.cpt > 0 ? p.cpt : 1);
-    int l_rem = c_begin - l_nb * p.cpt;
-    int l_left = c_end - c_begin;
-    const uint32_t* wp;
-    const uint16_t* sp;
-    const uint32_t* zp;
-    int wstep;
-    auto seek_tile = [&]() {  // pointers for chunk (l_nb, l_rem)
-        const int W = L.width(l_nb);
-        const int tc = t < W ? t : W - 1;
-        const int kb = l_rem >> 2;
-        wstep = W * 4;  // one chunk: W columns x 4 words
-        wp = p.qd + L.block_word(l_nb, kb) + ((size_t)(l_rem & 3) * W + tc) * 4;
-        const int n = 128 * l_nb + tc;
-        sp = p.scales + (size_t)kb * p.N + n;
-        zp = p.qzeros + (size_t)kb * (p.N / 8) + (n >> 3);
-    };
-    if (l_left > 0) seek_tile();
-    else {
-        wp = p.qd;
-        sp = p.scales;
-        zp = p.qzeros;
-        wstep = 0;
+    if (threadIdx.x < S) {
+        mbar_init(&full[threadIdx.x], 1);  // the producer's expect-tx arrival
+        fence_mbar_init();
+    } else if (threadIdx.x >= 32 && threadIdx.x < 32 + S) {
+        mbar_init(&empty[threadIdx.x - 32], kGemvConsumerWarps);  // one arrival per consumer warp
+        fence_mbar_init();
     }
-    auto next_chunk = [&]() -> ChunkData {
-        ChunkData d;
-        d.w = ld_stream_v4(wp);
-        d.s = __ldg(sp);
-        d.zw = __ldg(zp);
-        if (l_left > 1) {
-            --l_left;
-            ++l_rem;
-            if (l_rem == p.cpt) {  // next tile (rare, uniform across the warpgroup)
-                l_rem = 0;
-                ++l_nb;
-                seek_tile();
-            } else {
-                wp += wstep;
-                if ((l_rem & 3) == 0) {  // next group of 128 rows
-                    sp += p.N;
-                    zp += p.N / 8;
+    if (threadIdx.x == 64) sh_abort = 0;
+    __syncthreads();
+
+    if (warp == kGemvConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        // With static weights the first copies go out before waiting on the
+        // preceding grid (weights, scales and zeros are never written by it).
+        if (!p.prefetch) pdl_wait();
+        if (elect_one()) {
+            const bool zbulk = p.N % 32 == 0;  // zero rows 16-byte aligned: one bulk copy
+            int nb = ub / p.KB, kb = ub - nb * p.KB;
+            int s = 0, wraps = 0;  // the next copy is use number `wraps` of stage s
+            int issued = 0;
+            for (int u = ub; u < ue; ++u) {
+                // stage s is free once every consumer warp released its previous use
+                if (wraps > 0 && !mbar_wait(&empty[s], (uint32_t)(wraps - 1) & 1u, abort_flag, &g_gemv_status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const int W = L.width(nb);
+                unsigned char* st = ring + (size_t)s * kGemvStage;
+                const uint32_t* zsrc = p.qzeros + (size_t)kb * (p.N / 8) + 16 * nb;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)(W * 64 + W * 2 + (zbulk ? W / 2 : 0)));
+                bulk_g2s(st + kStageW, p.qd + L.block_word(nb, kb), (uint32_t)W * 64, &full[s]);
+                bulk_g2s(st + kStageS, p.scales + (size_t)kb * p.N + 128 * nb, (uint32_t)W * 2, &full[s]);
+                if (zbulk) {
+                    bulk_g2s(st + kStageZ, zsrc, (uint32_t)W / 2, &full[s]);
+                } else {
+                    for (int j = 0; j < W / 8; ++j) cp_async_4(st + kStageZ + 4 * j, zsrc + j);
+                    cp_async_mbar_arrive(&full[s]);
+                }
+                ++issued;
+                if (++s == S) {
+                    s = 0;
+                    ++wraps;
+                }
+                if (++kb == p.KB) {
+                    kb = 0;
+                    ++nb;
                 }
             }
-        } else {
-            l_left = 0;  // stay on the last chunk: later loads re-read it and are never used
+            // every copy issued must land before the CTA may exit
+            const int first = issued > S ? issued - S : 0;
+            for (int i = first; i < issued; ++i) (void)mbar_wait(&full[i % S], (i / S) & 1, nullptr, &g_gemv_status);
         }
-        return d;
-    };
-
-    // With static weights the first loads go out before waiting on the
-    // preceding grid; otherwise after it (x, y and the workspace are always
-    // touched only after the wait).
-    ChunkData buf[D];
-    if (p.prefetch) {
-#pragma unroll
-        for (int i = 0; i < D; ++i) buf[i] = next_chunk();
+        __syncwarp();
+        pdl_launch_dependents();
+        return;
     }
+
+    // ---------------------------------------------------------------- consumers
+    const int h = warp >> 2;               // warpgroup: rows 32h..32h+31 of every unit
+    const int t = (warp & 3) * 32 + lane;  // column within the tile
+    const int ct = threadIdx.x;            // 0..511
     pdl_wait();
-    if (!p.prefetch) {
+    {
+        // activations to shared memory (rows m >= M zero), then 32-row sums
+        const int nvec = p.M * p.K / 8;
+        const uint4* xg = reinterpret_cast<const uint4*>(p.x);
+        uint4* xv = reinterpret_cast<uint4*>(xs);
+        for (int i = ct; i < M * p.K / 8; i += 32 * kGemvConsumerWarps)
+            xv[i] = i < nvec ? __ldg(xg + i) : make_uint4(0, 0, 0, 0);
+        consumer_bar();
+        const int nk = p.K / 32;
+        for (int i = ct; i < M * nk; i += 32 * kGemvConsumerWarps) {
+            const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs) + (size_t)i * 16;  // 32 bf16
+            float a = 0.f, b = 0.f;
 #pragma unroll
-        for (int i = 0; i < D; ++i) buf[i] = next_chunk();
+            for (int e = 0; e < 16; e += 2) {
+                a += bf16lo(xr[e]) + bf16hi(xr[e]);
+                b += bf16lo(xr[e + 1]) + bf16hi(xr[e + 1]);
+            }
+            xsum[i] = a + b;
+        }
+        consumer_bar();
     }
     pdl_launch_dependents();  // one wave: the next grid can only start where this one ends
 
-    // activations to shared memory, then per-32-row chunk sums
-    {
-        const int nvec = p.M * p.K / 8;  // 16-byte vectors of x actually present
-        const uint4* xg = reinterpret_cast<const uint4*>(p.x);
-        uint4* xv = reinterpret_cast<uint4*>(xs);
-        for (int i = tid; i < M * p.K / 8; i += blockDim.x) xv[i] = i < nvec ? __ldg(xg + i) : make_uint4(0, 0, 0, 0);
-        __syncthreads();
-        const int nk = p.K / 32;
-        for (int i = tid; i < M * nk; i += blockDim.x) {
-            const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs) + (size_t)i * 16;  // 32 bf16
-            float s = 0.f;
+    const int nk = p.K / 32;
+    int nb = ub / p.KB, kb = ub - nb * p.KB;
+    int W = L.width(nb);
+    int tc = t < W ? t : W - 1;  // threads beyond a ragged tile read column W-1 and discard it
+    float acc[M];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const uint32_t v = xr[e];
-                s += bf16lo(v);
-                s += bf16hi(v);
-            }
-            xsum[i] = s;
-        }
-        __syncthreads();
-    }
-    if (!active) return;  // no named barrier is shared across warpgroups
-
-    // Tile segments: [seg_a, seg_b) lies in one tile.  Buffer slot i holds
-    // chunk c with (c - c_begin) % D == i, so segments walk the same D-groups.
-    int seg_a = c_begin;
-    int group_base = c_begin;
-    while (seg_a < c_end) {
-        const int nb = seg_a / p.cpt;
-        const int tile_end = (nb + 1) * p.cpt;
-        const int seg_b = c_end < tile_end ? c_end : tile_end;
-        const int n = 128 * nb + t;
-        const int zshift = 4 * (n & 7);
-        float acc[M];
+    for (int m = 0; m < M; ++m) acc[m] = 0.f;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int u = ub; u < ue; ++u) {
+        if (ok && !mbar_wait_warp(&full[s], ph, abort_flag, &g_gemv_status)) ok = false;
+        if (ok) {
+            const uint32_t st = smem_u32(ring + (size_t)s * kGemvStage);
+            const uint4 wv4 = lds_v4(st + kStageW + (uint32_t)((h * W + tc) * 16));
+            const float sc = f16_bits_to_f32((uint16_t)lds_u16(st + kStageS + (uint32_t)tc * 2));
+            const uint32_t zw = lds_u32(st + kStageZ + (uint32_t)(tc >> 3) * 4);
+            const float zoff = 128.f + (float)((zw >> (4 * (tc & 7))) & 0xFu);
+            const int k0 = kb * 128 + 32 * h;
+            const uint32_t wv[4] = {wv4.x, wv4.y, wv4.z, wv4.w};
+            float d[4][M];  // four independent chains per token (one per word)
 #pragma unroll
-        for (int m = 0; m < M; ++m) acc[m] = 0.f;
-        for (int base = group_base; base < seg_b; base += D) {
+            for (int j = 0; j < 4; ++j) {
+                uint32_t wp[4];
 #pragma unroll
-            for (int i = 0; i < D; ++i) {
-                const int c = base + i;
-                if (c >= seg_a && c < seg_b) {
-                    const ChunkData cur = buf[i];
-                    buf[i] = next_chunk();
-                    {
-                        const int rem = c - nb * p.cpt;
-                        const int k0 = (rem >> 2) * 128 + (rem & 3) * 32;
-                        const float s = f16_bits_to_f32((uint16_t)cur.s);
-                        const float zoff = 128.f + (float)((cur.zw >> zshift) & 0xFu);
-                        // four independent accumulation chains per token (one per word)
-                        float d[4][M];
-                        const uint32_t wv[4] = {cur.w.x, cur.w.y, cur.w.z, cur.w.w};
+                for (int qq = 0; qq < 4; ++qq) wp[qq] = magic_pair(wv[j], qq);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint32_t wp[4];
+                for (int m = 0; m < M; ++m) {
+                    const uint4 xq = *reinterpret_cast<const uint4*>(xs + (size_t)m * p.K + k0 + 8 * j);
+                    const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
+                    float a = 0.f;
 #pragma unroll
-                            for (int qq = 0; qq < 4; ++qq) wp[qq] = magic_pair(wv[j], qq);
-#pragma unroll
-                            for (int m = 0; m < M; ++m) {
-                                const uint4 xq = *reinterpret_cast<const uint4*>(xs + (size_t)m * p.K + k0 + 8 * j);
-                                const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
-                                float a = 0.f;
-#pragma unroll
-                                for (int qq = 0; qq < 4; ++qq) {
-                                    a = fma_lo(wp[qq], xp[qq], a);
-                                    a = fma_hi(wp[qq], xp[qq], a);
-                                }
-                                d[j][m] = a;
-                            }
-                        }
-                        const int kc = k0 >> 5;
-#pragma unroll
-                        for (int m = 0; m < M; ++m) {
-                            const float dot = (d[0][m] + d[1][m]) + (d[2][m] + d[3][m]);
-                            acc[m] = fmaf(s, fmaf(-zoff, xsum[m * (p.K / 32) + kc], dot), acc[m]);
-                        }
+                    for (int qq = 0; qq < 4; ++qq) {
+                        a = fma_lo(wp[qq], xp[qq], a);
+                        a = fma_hi(wp[qq], xp[qq], a);
                     }
+                    d[j][m] = a;
                 }
             }
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const float dot = (d[0][m] + d[1][m]) + (d[2][m] + d[3][m]);
+                acc[m] = fmaf(sc, fmaf(-zoff, xsum[m * nk + (k0 >> 5)], dot), acc[m]);
+            }
         }
-        gemv_flush<M>(p, worker, wg, t, nb, seg_a, seg_b, c_begin, acc, sh_last);
-        group_base = seg_b - (seg_b - c_begin) % D;
-        seg_a = seg_b;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
+        if (++s == S) {
+            s = 0;
+            ph ^= 1;
+        }
+        if (kb + 1 == p.KB || u + 1 == ue) {
+            // ---- end of a tile segment: add the warpgroups, write or hand on
+            const int t0u = nb * p.KB, t1u = t0u + p.KB;
+            const bool whole = ub <= t0u && ue >= t1u;
+            const int n = 128 * nb + t;
+#pragma unroll
+            for (int m = 0; m < M; ++m) red[(h * M + m) * 128 + t] = acc[m];
+            consumer_bar();
+            const int slot = ub >= t0u ? 0 : 1;  // the CTA's first tile, or its last
+            for (int m = h; m < M; m += 4) {
+                const float v = ((red[(0 * M + m) * 128 + t] + red[(1 * M + m) * 128 + t]) +
+                                 red[(2 * M + m) * 128 + t]) + red[(3 * M + m) * 128 + t];
+                if (whole) {
+                    if (t < W && m < p.M) p.y[(size_t)m * p.N + n] = f32_to_bf16_rn(v);
+                } else {
+                    p.partials[(((size_t)blockIdx.x * 2 + slot) * M + m) * 128 + t] = v;
+                }
+            }
+            if (!whole) {
+                __threadfence();
+                consumer_bar();
+                const int cf = cta_of(t0u, p), cl = cta_of(t1u - 1, p);
+                if (ct == 0) {
+                    const unsigned old = atomicAdd(&p.counters[nb], 1u);
+                    sh_last = (old == (unsigned)(cl - cf)) ? 1 : 0;
+                }
+                consumer_bar();
+                if (sh_last) {
+                    __threadfence();
+                    for (int m = h; m < M; m += 4) {
+                        float sum = 0.f;
+                        for (int c = cf; c <= cl; ++c) {  // fixed order: deterministic
+                            const int sl = cta_begin(c, p) >= t0u ? 0 : 1;
+                            sum += __ldcg(p.partials + (((size_t)c * 2 + sl) * M + m) * 128 + t);
+                        }
+                        if (t < W && m < p.M) p.y[(size_t)m * p.N + n] = f32_to_bf16_rn(sum);
+                    }
+                    if (ct == 0) p.counters[nb] = 0u;
+                }
+            }
+            consumer_bar();  // red and sh_last are reused by the next segment
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[m] = 0.f;
+        }
+        if (++kb == p.KB) {
+            kb = 0;
+            ++nb;
+            W = L.width(nb < L.NB ? nb : L.NB - 1);
+            tc = t < W ? t : W - 1;
+        }
     }
+    if (!ok) *abort_flag = 1;
 }
 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
-
 static int gemv_mtile(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
 
 bool gemv_plan(int M, int N, int K, int sms, GemvPlan* out) {
-    if (M < 1 || M > 8) return false;
+    if (M < 1 || M > 8 || sms < 1) return false;
     const int MT = gemv_mtile(M);
     const Layout L(K, N);
-    const long long C = (long long)L.NB * 4 * L.KB;
-    if (C >= (1ll << 31)) return false;
-    const size_t smem = (size_t)MT * K * 2 + (size_t)MT * (K / 32) * 4;
-    if (smem > (size_t)kGemvMaxSmem) return false;
+    const long long U = (long long)L.NB * L.KB;
+    if (U < 1 || U >= (1ll << 31)) return false;
     if ((size_t)L.NB > kMaxCounters) return false;
-    long long P = (long long)sms * kGemvWG;
-    if (P > C) P = C;
-    const int ctas = (int)((P + kGemvWG - 1) / kGemvWG);
+    const int ctas = (int)(U < sms ? U : sms);
+    const long long per = (U + ctas - 1) / ctas;  // most units of any CTA
+    const size_t fixed = GemvSmem(MT, K, 0).total;
+    const size_t per_stage = kGemvStage + 16;
+    if (fixed + 2 * per_stage > (size_t)kGemvMaxSmem) return false;
+    long long S = (long long)(((size_t)kGemvMaxSmem - fixed) / per_stage);
+    if (S > kGemvMaxStages) S = kGemvMaxStages;
+    if (S > per) S = per;
+    if (S < 2) S = 2;
     out->ctas = ctas;
-    out->P = (int)P;
-    out->C = C;
-    out->smem = smem;
-    out->ws_bytes = ws_counter_bytes(L.NB) + (size_t)P * 2 * MT * 128 * sizeof(float);
+    out->P = ctas;
+    out->C = U;
+    out->S = (int)S;
+    out->smem = GemvSmem(MT, K, (int)S).total;
+    out->ws_bytes = ws_counter_bytes(L.NB) + (size_t)ctas * 2 * MT * 128 * sizeof(float);
     return true;
 }
 
 template <int M>
 static cudaError_t launch_m(const GemvParams& prm, const GemvPlan& plan, cudaStream_t s, bool pdl) {
-    constexpr int D = M == 1 ? 8 : M == 2 ? 6 : M == 4 ? 4 : 2;  // chunks in flight per thread
-    auto kern = gemv_kernel<M, D>;
+    auto kern = gemv_kernel<M>;
     // the dynamic shared memory limit is raised once per device to the maximum
     // any plan asks for, so that launches (also inside graph capture) make no
     // other runtime calls
@@ -339,7 +345,7 @@ static cudaError_t launch_m(const GemvParams& prm, const GemvPlan& plan, cudaStr
         if (e != cudaSuccess) return e;
         set_for[dev] = 1;
     }
-    return launch_kernel(kern, dim3(plan.ctas), dim3(128 * kGemvWG), plan.smem, s, pdl, prm);
+    return launch_kernel(kern, dim3(plan.ctas), dim3(kGemvThreads), plan.smem, s, pdl, prm);
 }
 
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
@@ -359,11 +365,9 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qd, const uint16_t* s
     prm.K = K;
     prm.KB = L.KB;
     prm.NB = L.NB;
-    prm.cpt = 4 * L.KB;
-    prm.C = (int)plan.C;
-    prm.P = plan.P;
-    prm.q = (int)(plan.C / plan.P);
-    prm.r = (int)(plan.C % plan.P);
+    prm.q = (int)(plan.C / plan.ctas);
+    prm.r = (int)(plan.C % plan.ctas);
+    prm.S = plan.S;
     const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     switch (gemv_mtile(M)) {

@@ -14,8 +14,9 @@ cudaError_t launch_unpack(const uint32_t* qd, uint32_t* q, int K, int N, cudaStr
 
 // CUDA-core split-K GEMV (M <= 8)
 struct GemvPlan {
-    int ctas, P;     // CTAs, workers (warpgroups)
-    long long C;     // 2 KB chunks
+    int ctas, P;     // CTAs, range owners (one per CTA)
+    int S;           // shared-memory ring stages
+    long long C;     // units: one 128-row group of one 128-column tile
     size_t smem, ws_bytes;
 };
 bool gemv_plan(int M, int N, int K, int sms, GemvPlan* out);
