@@ -101,30 +101,39 @@ W4A16_DEVICE bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete sleeps until it
+// completes or `ns` nanoseconds pass, instead of returning at once: waiting
+// warps then take no issue slots from the working ones.
+W4A16_DEVICE bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Longest single sleep of a bounded wait (the abort flag and the clock are
+// checked between sleeps).
+constexpr uint32_t kSleepNs = 50000;
+
 // Bounded wait for the phase with the given parity to complete.  `abort` is a
 // shared flag: once any thread of the CTA has given up, the others stop
-// waiting at once.  A phase that has already completed costs one poll: the
-// flag is read only after a failed poll, and the clock only every 1024 polls.
+// waiting.  A phase that has already completed costs one poll; otherwise the
+// thread sleeps on the barrier between checks of the flag and the clock.
 // Returns false on timeout or abort.
 W4A16_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
                             uint64_t limit_ns = kWaitNs) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
-    if (abort && *abort) return false;
-    uint64_t t0 = 0;
+    const uint64_t t0 = globaltimer();
     for (uint32_t i = 0; i < kWaitSpins; ++i) {
-        if (mbar_try_wait(a, parity)) return true;
-        if ((i & 1023) == 1023) {
-            if (abort && *abort) return false;
-            const uint64_t now = globaltimer();
-            if (t0 == 0) {
-                t0 = now;
-            } else if (now - t0 > limit_ns) {
-                if (abort) *abort = 1;
-                atomicExch(status, (int)W4A16_ETIMEOUT);
-                return false;
-            }
-        }
+        if (abort && *abort) return false;
+        if (mbar_try_wait_sleep(a, parity, kSleepNs)) return true;
+        if (globaltimer() - t0 > limit_ns) break;
     }
     if (abort) *abort = 1;
     atomicExch(status, (int)W4A16_ETIMEOUT);

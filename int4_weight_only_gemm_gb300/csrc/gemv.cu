@@ -17,14 +17,15 @@
 // as the ring allows, so a CTA has most of its bytes requested at once and
 // the loads never wait on the arithmetic.
 //
-// Arithmetic: four consumer warpgroups; warpgroup h takes rows 32h..32h+31
-// of every unit and thread t column t: one 128-bit shared load gives its 32
-// codes.  Per token, dot = sum_k (128 + q_k) x_k with the bfloat16 value
-// 128 + q made by one mask-and-or per pair of rows (exact) and bf16 x bf16
-// -> f32 fused multiply-adds; then the zero point and scale are applied once
-// per 32 rows in f32: acc += s (dot - (128 + z) sum_k x_k), with the 32-row
-// activation sums computed once per CTA.  The scale is used at its full
-// binary16 precision.
+// Arithmetic: four consumer warpgroups take the CTA's units in turn (unit i
+// goes to warpgroup i % 4), thread t column t: four 128-bit shared loads give
+// its 128 codes, so one barrier wait, one release and one scale / zero step
+// serve 128 weights.  Per token, dot = sum_k (128 + q_k) x_k with the
+// bfloat16 value 128 + q made by one mask-and-or per pair of rows (exact) and
+// bf16 x bf16 -> f32 fused multiply-adds; then the zero point and scale are
+// applied once per group in f32: acc += s (dot - (128 + z) sum_k x_k), with
+// the per-group activation sums computed once per CTA.  The scale is used at
+// its full binary16 precision.
 //
 // Reduction: at the end of each tile segment the four warpgroups' sums are
 // added through shared memory in warpgroup order.  A tile that lies whole in
@@ -76,15 +77,17 @@ W4A16_DEVICE uint32_t lds_u16(uint32_t addr) {
     return v;
 }
 
-// Shared-memory layout (bytes from the dynamic base), identical on both sides.
+// Shared-memory layout (bytes from the dynamic base), identical on both
+// sides.  Every region starts on a 16-byte boundary (the mbarriers need 8).
 struct GemvSmem {
     size_t xs, xsum, red, bars, total;
+    static __host__ __device__ size_t up16(size_t v) { return (v + 15) & ~(size_t)15; }
     __host__ __device__ GemvSmem(int M, int K, int S) {
-        xs = (size_t)S * kGemvStage;                 // ring first (16-byte aligned stages)
-        xsum = xs + (size_t)M * K * 2;               // [M][K] bf16 activations
-        red = xsum + (size_t)M * (K / 32) * 4;       // [M][K/32] 32-row activation sums
-        bars = red + (size_t)4 * M * 128 * 4;        // [4][M][128] warpgroup partial sums
-        total = bars + (size_t)2 * S * 8;            // full[S], empty[S]
+        xs = (size_t)S * kGemvStage;                    // ring first (16-byte aligned stages)
+        xsum = up16(xs + (size_t)M * K * 2);            // [M][K] bf16 activations
+        red = up16(xsum + (size_t)M * (K / 128) * 4);   // [M][K/128] per-group activation sums
+        bars = up16(red + (size_t)4 * M * 128 * 4);     // [4][M][128] warpgroup partial sums
+        total = bars + (size_t)2 * S * 8;               // full[S], empty[S]
     }
 };
 
@@ -112,7 +115,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
         mbar_init(&full[threadIdx.x], 1);  // the producer's expect-tx arrival
         fence_mbar_init();
     } else if (threadIdx.x >= 32 && threadIdx.x < 32 + S) {
-        mbar_init(&empty[threadIdx.x - 32], kGemvConsumerWarps);  // one arrival per consumer warp
+        mbar_init(&empty[threadIdx.x - 32], 4);  // one arrival per warp of the consuming warpgroup
         fence_mbar_init();
     }
     if (threadIdx.x == 64) sh_abort = 0;
@@ -166,24 +169,23 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     }
 
     // ---------------------------------------------------------------- consumers
-    const int h = warp >> 2;               // warpgroup: rows 32h..32h+31 of every unit
+    const int wg = warp >> 2;              // warpgroup 0..3: takes the CTA's units i with i % 4 == wg
     const int t = (warp & 3) * 32 + lane;  // column within the tile
     const int ct = threadIdx.x;            // 0..511
     pdl_wait();
     {
-        // activations to shared memory (rows m >= M zero), then 32-row sums
+        // activations to shared memory (rows m >= M zero), then per-group sums
         const int nvec = p.M * p.K / 8;
         const uint4* xg = reinterpret_cast<const uint4*>(p.x);
         uint4* xv = reinterpret_cast<uint4*>(xs);
         for (int i = ct; i < M * p.K / 8; i += 32 * kGemvConsumerWarps)
             xv[i] = i < nvec ? __ldg(xg + i) : make_uint4(0, 0, 0, 0);
         consumer_bar();
-        const int nk = p.K / 32;
-        for (int i = ct; i < M * nk; i += 32 * kGemvConsumerWarps) {
-            const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs) + (size_t)i * 16;  // 32 bf16
+        for (int i = ct; i < M * p.KB; i += 32 * kGemvConsumerWarps) {
+            const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs) + (size_t)i * 64;  // 128 bf16
             float a = 0.f, b = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
+#pragma unroll 8
+            for (int e = 0; e < 64; e += 2) {
                 a += bf16lo(xr[e]) + bf16hi(xr[e]);
                 b += bf16lo(xr[e + 1]) + bf16hi(xr[e + 1]);
             }
@@ -193,67 +195,112 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     }
     pdl_launch_dependents();  // one wave: the next grid can only start where this one ends
 
-    const int nk = p.K / 32;
-    int nb = ub / p.KB, kb = ub - nb * p.KB;
-    int W = L.width(nb);
-    int tc = t < W ? t : W - 1;  // threads beyond a ragged tile read column W-1 and discard it
-    float acc[M];
-#pragma unroll
-    for (int m = 0; m < M; ++m) acc[m] = 0.f;
-    int s = 0;
+    // 32-bit shared addresses
+    const uint32_t ring_a = smem_u32(smem);
+    const uint32_t xs_a = ring_a + (uint32_t)lay.xs;
+    const uint32_t xsum_a = ring_a + (uint32_t)lay.xsum;
+    const uint32_t full_a = ring_a + (uint32_t)lay.bars;  // full[s] at full_a + 8 s
+    const uint32_t empty_a = full_a + 8u * (uint32_t)S;
+    const uint32_t xrow = (uint32_t)p.K * 2;             // bytes between token rows of xs
+    const uint32_t srow = (uint32_t)p.KB * 4;            // bytes between token rows of xsum
+    // independent accumulation chains per 32-row chunk and token: one per
+    // word for few tokens, one per chunk when the tokens already give the ILP
+    constexpr int NCH = M <= 2 ? 4 : 1;
+    int i = wg;  // this warpgroup's next unit, relative to the CTA's first
+    int s = wg;  // its stage (S >= 4)
     uint32_t ph = 0;
     bool ok = true;
-    for (int u = ub; u < ue; ++u) {
-        if (ok && !mbar_wait_warp(&full[s], ph, abort_flag, &g_gemv_status)) ok = false;
-        if (ok) {
-            const uint32_t st = smem_u32(ring + (size_t)s * kGemvStage);
-            const uint4 wv4 = lds_v4(st + kStageW + (uint32_t)((h * W + tc) * 16));
-            const float sc = f16_bits_to_f32((uint16_t)lds_u16(st + kStageS + (uint32_t)tc * 2));
-            const uint32_t zw = lds_u32(st + kStageZ + (uint32_t)(tc >> 3) * 4);
-            const float zoff = 128.f + (float)((zw >> (4 * (tc & 7))) & 0xFu);
-            const int k0 = kb * 128 + 32 * h;
-            const uint32_t wv[4] = {wv4.x, wv4.y, wv4.z, wv4.w};
-            float d[4][M];  // four independent chains per token (one per word)
+    int u = ub;
+    int nb = ub / p.KB;
+    while (u < ue) {
+        // ---- one tile segment: units [u, seg_end) of tile nb
+        const int seg_end = ue < (nb + 1) * p.KB ? ue : (nb + 1) * p.KB;
+        const int W = L.width(nb);
+        const int tc = t < W ? t : W - 1;  // threads beyond a ragged tile read column W-1 and discard it
+        const uint32_t w_off = (uint32_t)tc * 16;
+        const uint32_t cstep = (uint32_t)W * 16;  // bytes between the unit's 32-row chunks
+        const uint32_t s_off = kStageS + (uint32_t)tc * 2;
+        const uint32_t z_off = kStageZ + (uint32_t)(tc >> 3) * 4;
+        const uint32_t zsh = 4u * (uint32_t)(tc & 7);
+        const int t0u = nb * p.KB;
+        float acc[M];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t wp[4];
+        for (int m = 0; m < M; ++m) acc[m] = 0.f;
+        for (; ub + i < seg_end; i += 4) {
+            const int kb = ub + i - t0u;
+            const uint32_t st_a = ring_a + (uint32_t)s * kGemvStage;
+            if (ok) {
+                const bool ready = mbar_try_wait(full_a + 8u * (uint32_t)s, ph);
+                if (!__all_sync(0xFFFFFFFFu, ready) &&
+                    !mbar_wait_warp(&full[s], ph, abort_flag, &g_gemv_status))
+                    ok = false;
+            }
+            if (ok) {
+                uint4 wc[4];
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq) wp[qq] = magic_pair(wv[j], qq);
+                for (int c = 0; c < 4; ++c) wc[c] = lds_v4(st_a + w_off + (uint32_t)c * cstep);
+                const float sc = f16_bits_to_f32((uint16_t)lds_u16(st_a + s_off));
+                const uint32_t zw = lds_u32(st_a + z_off);
+                const float zoff = 128.f + (float)((zw >> zsh) & 0xFu);
+                const uint32_t x_a = xs_a + (uint32_t)kb * 256;
+                float d[4 * NCH][M];
+#pragma unroll
+                for (int c = 0; c < 4 * NCH; ++c)
+#pragma unroll
+                    for (int m = 0; m < M; ++m) d[c][m] = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t wv[4] = {wc[c].x, wc[c].y, wc[c].z, wc[c].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {  // word j of chunk c: rows 32c + 8j .. +7
+                        const int ci = c * NCH + j % NCH;
+                        uint32_t wp[4];
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq) wp[qq] = magic_pair(wv[j], qq);
+#pragma unroll
+                        for (int m = 0; m < M; ++m) {
+                            const uint4 xq = lds_v4(x_a + (uint32_t)m * xrow + (uint32_t)(64 * c + 16 * j));
+                            const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
+                            float a = d[ci][m];
+#pragma unroll
+                            for (int qq = 0; qq < 4; ++qq) {
+                                a = fma_lo(wp[qq], xp[qq], a);
+                                a = fma_hi(wp[qq], xp[qq], a);
+                            }
+                            d[ci][m] = a;
+                        }
+                    }
+                }
+                const uint32_t xz_a = xsum_a + (uint32_t)kb * 4;
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
-                    const uint4 xq = *reinterpret_cast<const uint4*>(xs + (size_t)m * p.K + k0 + 8 * j);
-                    const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
-                    float a = 0.f;
+                    // pairwise sum of the chains
 #pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) {
-                        a = fma_lo(wp[qq], xp[qq], a);
-                        a = fma_hi(wp[qq], xp[qq], a);
-                    }
-                    d[j][m] = a;
+                    for (int w2 = 1; w2 < 4 * NCH; w2 *= 2)
+#pragma unroll
+                        for (int c = 0; c + w2 < 4 * NCH; c += 2 * w2) d[c][m] += d[c + w2][m];
+                    const float xz = __uint_as_float(lds_u32(xz_a + (uint32_t)m * srow));
+                    acc[m] = fmaf(sc, fmaf(-zoff, xz, d[0][m]), acc[m]);
                 }
             }
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-                const float dot = (d[0][m] + d[1][m]) + (d[2][m] + d[3][m]);
-                acc[m] = fmaf(sc, fmaf(-zoff, xsum[m * nk + (k0 >> 5)], dot), acc[m]);
+            // this warp is done with the stage (its shared loads have returned)
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty_a + 8u * (uint32_t)s) : "memory");
+            s += 4;
+            if (s >= S) {
+                s -= S;
+                ph ^= 1;
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
-        if (++s == S) {
-            s = 0;
-            ph ^= 1;
-        }
-        if (kb + 1 == p.KB || u + 1 == ue) {
-            // ---- end of a tile segment: add the warpgroups, write or hand on
-            const int t0u = nb * p.KB, t1u = t0u + p.KB;
+        // ---- end of the segment: add the warpgroups, write or hand on
+        {
+            const int t1u = t0u + p.KB;
             const bool whole = ub <= t0u && ue >= t1u;
             const int n = 128 * nb + t;
 #pragma unroll
-            for (int m = 0; m < M; ++m) red[(h * M + m) * 128 + t] = acc[m];
+            for (int m = 0; m < M; ++m) red[(wg * M + m) * 128 + t] = acc[m];
             consumer_bar();
             const int slot = ub >= t0u ? 0 : 1;  // the CTA's first tile, or its last
-            for (int m = h; m < M; m += 4) {
+            for (int m = wg; m < M; m += 4) {
                 const float v = ((red[(0 * M + m) * 128 + t] + red[(1 * M + m) * 128 + t]) +
                                  red[(2 * M + m) * 128 + t]) + red[(3 * M + m) * 128 + t];
                 if (whole) {
@@ -273,11 +320,24 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
                 consumer_bar();
                 if (sh_last) {
                     __threadfence();
-                    for (int m = h; m < M; m += 4) {
+                    for (int m = wg; m < M; m += 4) {
+                        // all partials requested before any is added; then added in CTA order
+                        constexpr int kBatch = 8;
                         float sum = 0.f;
-                        for (int c = cf; c <= cl; ++c) {  // fixed order: deterministic
-                            const int sl = cta_begin(c, p) >= t0u ? 0 : 1;
-                            sum += __ldcg(p.partials + (((size_t)c * 2 + sl) * M + m) * 128 + t);
+                        for (int c0 = cf; c0 <= cl; c0 += kBatch) {
+                            float v[kBatch];
+#pragma unroll
+                            for (int i = 0; i < kBatch; ++i) {
+                                const int c = c0 + i;
+                                v[i] = 0.f;
+                                if (c <= cl) {
+                                    const int sl = cta_begin(c, p) >= t0u ? 0 : 1;
+                                    v[i] = __ldcg(p.partials + (((size_t)c * 2 + sl) * M + m) * 128 + t);
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < kBatch; ++i)
+                                if (c0 + i <= cl) sum += v[i];
                         }
                         if (t < W && m < p.M) p.y[(size_t)m * p.N + n] = f32_to_bf16_rn(sum);
                     }
@@ -285,15 +345,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
                 }
             }
             consumer_bar();  // red and sh_last are reused by the next segment
-#pragma unroll
-            for (int m = 0; m < M; ++m) acc[m] = 0.f;
         }
-        if (++kb == p.KB) {
-            kb = 0;
-            ++nb;
-            W = L.width(nb < L.NB ? nb : L.NB - 1);
-            tc = t < W ? t : W - 1;
-        }
+        u = seg_end;
+        ++nb;
     }
     if (!ok) *abort_flag = 1;
 }
@@ -315,16 +369,19 @@ bool gemv_plan(int M, int N, int K, int sms, GemvPlan* out) {
     const long long per = (U + ctas - 1) / ctas;  // most units of any CTA
     const size_t fixed = GemvSmem(MT, K, 0).total;
     const size_t per_stage = kGemvStage + 16;
-    if (fixed + 2 * per_stage > (size_t)kGemvMaxSmem) return false;
+    if (fixed + 4 * per_stage > (size_t)kGemvMaxSmem) return false;
     long long S = (long long)(((size_t)kGemvMaxSmem - fixed) / per_stage);
     if (S > kGemvMaxStages) S = kGemvMaxStages;
     if (S > per) S = per;
-    if (S < 2) S = 2;
+    if (S < 4) S = 4;  // four warpgroups each hold a stage
+    if (fixed + (size_t)S * per_stage > (size_t)kGemvMaxSmem) return false;
     out->ctas = ctas;
     out->P = ctas;
     out->C = U;
     out->S = (int)S;
-    out->smem = GemvSmem(MT, K, (int)S).total;
+    const GemvSmem lay(MT, K, (int)S);
+    if (lay.xsum % 16 || lay.red % 16 || lay.bars % 16) return false;  // never: regions are rounded up
+    out->smem = lay.total;
     out->ws_bytes = ws_counter_bytes(L.NB) + (size_t)ctas * 2 * MT * 128 * sizeof(float);
     return true;
 }
