@@ -11,11 +11,13 @@
 // order.  Each CTA (one per SM) takes a contiguous range of equal length, so
 // every SM streams the same number of bytes.
 //
-// Data movement: a producer warp copies whole units -- packed weights, the
-// group's fp16 scales and zero words -- into a ring of shared-memory stages
-// with bulk asynchronous copies (mbarrier transaction counts), as far ahead
-// as the ring allows, so a CTA has most of its bytes requested at once and
-// the loads never wait on the arithmetic.
+// Data movement: a producer warp copies the packed weights of whole units
+// into a ring of shared-memory stages, one bulk asynchronous copy per unit
+// (mbarrier transaction counts), as far ahead as the ring allows, so a CTA
+// has most of its bytes requested at once and the loads never wait on the
+// arithmetic.  The copy engine keeps only a few copies in flight per SM, so
+// a unit is one copy: each thread loads its column's fp16 scale and zero
+// word itself, two units ahead of use.
 //
 // Arithmetic: four consumer warpgroups take the CTA's units in turn (unit i
 // goes to warpgroup i % 4), thread t column t: four 128-bit shared loads give
@@ -55,10 +57,7 @@ struct GemvParams {
 
 constexpr int kGemvConsumerWarps = 16;                       // four warpgroups
 constexpr int kGemvThreads = 32 * (kGemvConsumerWarps + 1);  // plus the producer warp
-constexpr int kStageW = 0;                                   // packed weights, W * 64 bytes
-constexpr int kStageS = 8192;                                // fp16 scales, W * 2 bytes
-constexpr int kStageZ = 8192 + 256;                          // zero words, W / 2 bytes
-constexpr int kGemvStage = 8192 + 256 + 64;
+constexpr int kGemvStage = 8192;                             // packed weights of one unit, W * 64 bytes
 constexpr int kGemvMaxStages = 32;
 constexpr int kGemvMaxSmem = 226 * 1024;
 
@@ -70,12 +69,6 @@ __device__ __forceinline__ int cta_of(int u, const GemvParams& p) {
 }
 
 __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kGemvConsumerWarps) : "memory"); }
-
-W4A16_DEVICE uint32_t lds_u16(uint32_t addr) {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-    return v;
-}
 
 // Shared-memory layout (bytes from the dynamic base), identical on both
 // sides.  Every region starts on a 16-byte boundary (the mbarriers need 8).
@@ -127,7 +120,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
         // preceding grid (weights, scales and zeros are never written by it).
         if (!p.prefetch) pdl_wait();
         if (elect_one()) {
-            const bool zbulk = p.N % 32 == 0;  // zero rows 16-byte aligned: one bulk copy
             int nb = ub / p.KB, kb = ub - nb * p.KB;
             int s = 0, wraps = 0;  // the next copy is use number `wraps` of stage s
             int issued = 0;
@@ -138,17 +130,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
                     break;
                 }
                 const int W = L.width(nb);
-                unsigned char* st = ring + (size_t)s * kGemvStage;
-                const uint32_t* zsrc = p.qzeros + (size_t)kb * (p.N / 8) + 16 * nb;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(W * 64 + W * 2 + (zbulk ? W / 2 : 0)));
-                bulk_g2s(st + kStageW, p.qd + L.block_word(nb, kb), (uint32_t)W * 64, &full[s]);
-                bulk_g2s(st + kStageS, p.scales + (size_t)kb * p.N + 128 * nb, (uint32_t)W * 2, &full[s]);
-                if (zbulk) {
-                    bulk_g2s(st + kStageZ, zsrc, (uint32_t)W / 2, &full[s]);
-                } else {
-                    for (int j = 0; j < W / 8; ++j) cp_async_4(st + kStageZ + 4 * j, zsrc + j);
-                    cp_async_mbar_arrive(&full[s]);
-                }
+                mbar_arrive_expect_tx(&full[s], (uint32_t)W * 64);
+                bulk_g2s(ring + (size_t)s * kGemvStage, p.qd + L.block_word(nb, kb), (uint32_t)W * 64, &full[s]);
                 ++issued;
                 if (++s == S) {
                     s = 0;
@@ -208,6 +191,29 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     constexpr int NCH = M <= 2 ? 4 : 1;
     int i = wg;  // this warpgroup's next unit, relative to the CTA's first
     int s = wg;  // its stage (S >= 4)
+    // scale and zero word of this thread's column for the warpgroup's units,
+    // loaded two units ahead of use: (sc0, zw0) for unit i, (sc1, zw1) for i + 4
+    int pv = ub + wg;  // next unit to fetch
+    int pnb = pv / p.KB, pkb = pv - pnb * p.KB;
+    auto fetch = [&](uint16_t& sc, uint32_t& zw) {
+        if (pv < ue) {
+            const int Wp = L.width(pnb);
+            const int tp = t < Wp ? t : Wp - 1;
+            const int n = 128 * pnb + tp;
+            sc = __ldg(p.scales + (size_t)pkb * p.N + n);
+            zw = __ldg(p.qzeros + (size_t)pkb * (p.N / 8) + (n >> 3));
+        }
+        pv += 4;
+        pkb += 4;
+        while (pkb >= p.KB) {
+            pkb -= p.KB;
+            ++pnb;
+        }
+    };
+    uint16_t sc0 = 0, sc1 = 0;
+    uint32_t zw0 = 0, zw1 = 0;
+    fetch(sc0, zw0);
+    fetch(sc1, zw1);
     uint32_t ph = 0;
     bool ok = true;
     int u = ub;
@@ -219,8 +225,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
         const int tc = t < W ? t : W - 1;  // threads beyond a ragged tile read column W-1 and discard it
         const uint32_t w_off = (uint32_t)tc * 16;
         const uint32_t cstep = (uint32_t)W * 16;  // bytes between the unit's 32-row chunks
-        const uint32_t s_off = kStageS + (uint32_t)tc * 2;
-        const uint32_t z_off = kStageZ + (uint32_t)(tc >> 3) * 4;
         const uint32_t zsh = 4u * (uint32_t)(tc & 7);
         const int t0u = nb * p.KB;
         float acc[M];
@@ -239,9 +243,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
                 uint4 wc[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) wc[c] = lds_v4(st_a + w_off + (uint32_t)c * cstep);
-                const float sc = f16_bits_to_f32((uint16_t)lds_u16(st_a + s_off));
-                const uint32_t zw = lds_u32(st_a + z_off);
-                const float zoff = 128.f + (float)((zw >> zsh) & 0xFu);
+                const float sc = f16_bits_to_f32(sc0);
+                const float zoff = 128.f + (float)((zw0 >> zsh) & 0xFu);
                 const uint32_t x_a = xs_a + (uint32_t)kb * 256;
                 float d[4 * NCH][M];
 #pragma unroll
@@ -283,6 +286,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
                     acc[m] = fmaf(sc, fmaf(-zoff, xz, d[0][m]), acc[m]);
                 }
             }
+            sc0 = sc1;
+            zw0 = zw1;
+            fetch(sc1, zw1);
             // this warp is done with the stage (its shared loads have returned)
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty_a + 8u * (uint32_t)s) : "memory");
             s += 4;
