@@ -422,15 +422,20 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < CW; j += 4)
                         part[j / 4] = make_float4(acc[j / 2].x, acc[j / 2].y, acc[j / 2 + 1].x, acc[j / 2 + 1].y);
-                    __threadfence();
+                    // hand-off: the barrier orders the warpgroups' partial stores
+                    // before one thread, whose gpu-scope fence publishes them
+                    // with its arrival; the last arrival fences again before
+                    // the barrier that releases the reduction
                     asm volatile("bar.sync 5, %0;" ::"r"(128 * R) : "memory");
                     if (rt == 0) {
+                        __threadfence();
                         const unsigned old = atomicAdd(&p.counters[tile], 1u);
-                        *sh_last = (old == (unsigned)p.splits - 1) ? 1 : 0;
+                        const int last = old == (unsigned)p.splits - 1;
+                        if (last) __threadfence();
+                        *sh_last = last;
                     }
                     asm volatile("bar.sync 5, %0;" ::"r"(128 * R) : "memory");
                     if (*sh_last) {
-                        __threadfence();
                         // every split's values for this thread, summed in split order,
                         // 16 tokens at a time
                         const float4* base = reinterpret_cast<const float4*>(p.partials + ((size_t)tile * p.splits * 128 + t) * NT + r * CW);

@@ -8,8 +8,11 @@
 //
 // Work split: a unit is one 128-row group of K of one 128-column tile (8 KB
 // of packed weights, contiguous in the device layout), units in (tile, K)
-// order.  Each CTA (one per SM) takes a contiguous range of equal length, so
-// every SM streams the same number of bytes.
+// order, one CTA per SM.  With at least as many tiles as CTAs, each CTA takes
+// a range of whole tiles.  With fewer, each tile is cut into P/T pieces
+// (rounded down or up, P CTAs, T tiles) of contiguous units, one CTA per
+// piece: every CTA then streams about the same number of bytes and ends with
+// exactly one tile segment, so no CTA stops mid-stream to hand on a tile.
 //
 // Data movement: a producer warp copies the packed weights of whole units
 // into a ring of shared-memory stages, one bulk asynchronous copy per unit
@@ -50,7 +53,8 @@ struct GemvParams {
     uint32_t* counters;
     float* partials;
     int M, N, K, KB, NB;
-    int q, r;       // U = NB * KB units = q * gridDim.x + r: CTA b takes q units, plus one if b < r
+    int split;      // 0: CTA b takes tiles [b NB / P, (b+1) NB / P); 1: tiles are cut into pieces
+    int base, extra;  // split: tile t has base + (t < extra) pieces; CTAs are numbered tile by tile
     int S;          // ring stages
     int prefetch;   // weights may be loaded before the preceding grid completes
 };
@@ -61,11 +65,32 @@ constexpr int kGemvStage = 8192;                             // packed weights o
 constexpr int kGemvMaxStages = 32;
 constexpr int kGemvMaxSmem = 226 * 1024;
 
-// Division-free equal split of the units over the CTAs.
-__device__ __forceinline__ int cta_begin(int b, const GemvParams& p) { return b * p.q + (b < p.r ? b : p.r); }
-__device__ __forceinline__ int cta_of(int u, const GemvParams& p) {
-    const int big = p.r * (p.q + 1);
-    return u < big ? u / (p.q + 1) : p.r + (u - big) / p.q;
+// Pieces of tile t, and the first CTA of tile t (split mode).
+__device__ __forceinline__ int tile_pieces(int t, const GemvParams& p) { return p.base + (t < p.extra ? 1 : 0); }
+__device__ __forceinline__ int tile_first_cta(int t, const GemvParams& p) {
+    return t * p.base + (t < p.extra ? t : p.extra);
+}
+// The CTA's range of units [ub, ue).
+__device__ __forceinline__ void cta_range(int b, const GemvParams& p, int& ub, int& ue) {
+    if (!p.split) {
+        const int P = (int)gridDim.x;
+        ub = (int)((long long)b * p.NB / P) * p.KB;
+        ue = (int)((long long)(b + 1) * p.NB / P) * p.KB;
+        return;
+    }
+    const int big = p.extra * (p.base + 1);  // CTAs of the tiles with one piece more
+    int t, j, s;
+    if (b < big) {
+        t = b / (p.base + 1);
+        j = b - t * (p.base + 1);
+        s = p.base + 1;
+    } else {
+        t = p.extra + (b - big) / p.base;
+        j = (b - big) - (t - p.extra) * p.base;
+        s = p.base;
+    }
+    ub = t * p.KB + (j * p.KB) / s;
+    ue = t * p.KB + ((j + 1) * p.KB) / s;
 }
 
 __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kGemvConsumerWarps) : "memory"); }
@@ -101,8 +126,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const Layout L(p.K, p.N);
-    const int ub = cta_begin(blockIdx.x, p);
-    const int ue = cta_begin(blockIdx.x + 1, p);
+    int ub, ue;
+    cta_range(blockIdx.x, p, ub, ue);
 
     if (threadIdx.x < S) {
         mbar_init(&full[threadIdx.x], 1);  // the producer's expect-tx arrival
@@ -305,27 +330,31 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
 #pragma unroll
             for (int m = 0; m < M; ++m) red[(wg * M + m) * 128 + t] = acc[m];
             consumer_bar();
-            const int slot = ub >= t0u ? 0 : 1;  // the CTA's first tile, or its last
             for (int m = wg; m < M; m += 4) {
                 const float v = ((red[(0 * M + m) * 128 + t] + red[(1 * M + m) * 128 + t]) +
                                  red[(2 * M + m) * 128 + t]) + red[(3 * M + m) * 128 + t];
                 if (whole) {
                     if (t < W && m < p.M) p.y[(size_t)m * p.N + n] = f32_to_bf16_rn(v);
                 } else {
-                    p.partials[(((size_t)blockIdx.x * 2 + slot) * M + m) * 128 + t] = v;
+                    p.partials[((size_t)blockIdx.x * M + m) * 128 + t] = v;  // one partial per CTA
                 }
             }
             if (!whole) {
-                __threadfence();
+                // Hand-off: the barrier orders the CTA's partial stores before
+                // thread 0, whose gpu-scope fence publishes them with its
+                // arrival; the last arrival's fence makes every CTA's
+                // partials visible to this CTA after the next barrier.
                 consumer_bar();
-                const int cf = cta_of(t0u, p), cl = cta_of(t1u - 1, p);
+                const int cf = tile_first_cta(nb, p), cl = cf + tile_pieces(nb, p) - 1;
                 if (ct == 0) {
+                    __threadfence();
                     const unsigned old = atomicAdd(&p.counters[nb], 1u);
-                    sh_last = (old == (unsigned)(cl - cf)) ? 1 : 0;
+                    const int last = old == (unsigned)(cl - cf);
+                    if (last) __threadfence();
+                    sh_last = last;
                 }
                 consumer_bar();
                 if (sh_last) {
-                    __threadfence();
                     for (int m = wg; m < M; m += 4) {
                         // all partials requested before any is added; then added in CTA order
                         constexpr int kBatch = 8;
@@ -336,10 +365,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
                             for (int i = 0; i < kBatch; ++i) {
                                 const int c = c0 + i;
                                 v[i] = 0.f;
-                                if (c <= cl) {
-                                    const int sl = cta_begin(c, p) >= t0u ? 0 : 1;
-                                    v[i] = __ldcg(p.partials + (((size_t)c * 2 + sl) * M + m) * 128 + t);
-                                }
+                                if (c <= cl) v[i] = __ldcg(p.partials + ((size_t)c * M + m) * 128 + t);
                             }
 #pragma unroll
                             for (int i = 0; i < kBatch; ++i)
@@ -371,8 +397,24 @@ bool gemv_plan(int M, int N, int K, int sms, GemvPlan* out) {
     const long long U = (long long)L.NB * L.KB;
     if (U < 1 || U >= (1ll << 31)) return false;
     if ((size_t)L.NB > kMaxCounters) return false;
-    const int ctas = (int)(U < sms ? U : sms);
-    const long long per = (U + ctas - 1) / ctas;  // most units of any CTA
+    int ctas, split = 0, base = 0, extra = 0;
+    long long per;  // most units of any CTA
+    if (L.NB >= sms) {
+        ctas = sms;
+        per = (long long)((L.NB + sms - 1) / sms) * L.KB;
+    } else {
+        split = 1;
+        if ((long long)L.NB * L.KB <= sms) {  // one unit per CTA
+            base = L.KB;
+            extra = 0;
+            ctas = L.NB * L.KB;
+        } else {
+            base = sms / L.NB;  // < KB here
+            extra = sms % L.NB;
+            ctas = sms;
+        }
+        per = (L.KB + base - 1) / base;
+    }
     const size_t fixed = GemvSmem(MT, K, 0).total;
     const size_t per_stage = kGemvStage + 16;
     if (fixed + 4 * per_stage > (size_t)kGemvMaxSmem) return false;
@@ -381,14 +423,17 @@ bool gemv_plan(int M, int N, int K, int sms, GemvPlan* out) {
     if (S > per) S = per;
     if (S < 4) S = 4;  // four warpgroups each hold a stage
     if (fixed + (size_t)S * per_stage > (size_t)kGemvMaxSmem) return false;
+    const GemvSmem lay(MT, K, (int)S);
+    if (lay.xsum % 16 || lay.red % 16 || lay.bars % 16) return false;  // never: regions are rounded up
     out->ctas = ctas;
     out->P = ctas;
     out->C = U;
     out->S = (int)S;
-    const GemvSmem lay(MT, K, (int)S);
-    if (lay.xsum % 16 || lay.red % 16 || lay.bars % 16) return false;  // never: regions are rounded up
+    out->split = split;
+    out->base = base;
+    out->extra = extra;
     out->smem = lay.total;
-    out->ws_bytes = ws_counter_bytes(L.NB) + (size_t)ctas * 2 * MT * 128 * sizeof(float);
+    out->ws_bytes = ws_counter_bytes(L.NB) + (size_t)ctas * MT * 128 * sizeof(float);
     return true;
 }
 
@@ -428,8 +473,9 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qd, const uint16_t* s
     prm.K = K;
     prm.KB = L.KB;
     prm.NB = L.NB;
-    prm.q = (int)(plan.C / plan.ctas);
-    prm.r = (int)(plan.C % plan.ctas);
+    prm.split = plan.split;
+    prm.base = plan.base;
+    prm.extra = plan.extra;
     prm.S = plan.S;
     const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;

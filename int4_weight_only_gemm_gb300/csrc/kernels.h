@@ -16,6 +16,7 @@ cudaError_t launch_unpack(const uint32_t* qd, uint32_t* q, int K, int N, cudaStr
 struct GemvPlan {
     int ctas, P;     // CTAs, range owners (one per CTA)
     int S;           // shared-memory ring stages
+    int split, base, extra;  // unit partition (see gemv.cu)
     long long C;     // units: one 128-row group of one 128-column tile
     size_t smem, ws_bytes;
 };
