@@ -105,7 +105,7 @@ struct GemvSmem {
         xsum = up16(xs + (size_t)M * K * 2);            // [M][K] bf16 activations
         red = up16(xsum + (size_t)M * (K / 128) * 4);   // [M][K/128] per-group activation sums
         bars = up16(red + (size_t)4 * M * 128 * 4);     // [4][M][128] warpgroup partial sums
-        total = bars + (size_t)2 * S * 8;               // full[S], empty[S]
+        total = bars + (size_t)(2 * S + 1) * 8;         // full[S], empty[S], activations landed
     }
 };
 
@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     float* red = reinterpret_cast<float*>(smem + lay.red);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
     uint64_t* empty = full + S;
+    uint64_t* xbar = empty + S;
     __shared__ int sh_abort, sh_last;
     volatile int* abort_flag = &sh_abort;
 
@@ -136,19 +137,33 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
         mbar_init(&empty[threadIdx.x - 32], 4);  // one arrival per warp of the consuming warpgroup
         fence_mbar_init();
     }
-    if (threadIdx.x == 64) sh_abort = 0;
+    if (threadIdx.x == 64) {
+        sh_abort = 0;
+        mbar_init(xbar, 1);  // the producer's expect-tx arrival for the activation copy
+        fence_mbar_init();
+    }
     __syncthreads();
 
     if (warp == kGemvConsumerWarps) {
         // ------------------------------------------------------------ producer
-        // With static weights the first copies go out before waiting on the
-        // preceding grid (weights, scales and zeros are never written by it).
-        if (!p.prefetch) pdl_wait();
+        // The activations (written by the preceding grid) are one bulk copy,
+        // the first thing sent once that grid has completed.  With static
+        // weights a ring-full of weight copies goes out before that wait
+        // (weights, scales and zeros are never written by the preceding grid).
         if (elect_one()) {
+            bool x_sent = false;
+            auto send_x = [&]() {
+                pdl_wait();
+                mbar_arrive_expect_tx(xbar, (uint32_t)p.M * p.K * 2);
+                bulk_g2s(xs, p.x, (uint32_t)p.M * p.K * 2, xbar);
+                x_sent = true;
+            };
+            if (!p.prefetch) send_x();
             int nb = ub / p.KB, kb = ub - nb * p.KB;
             int s = 0, wraps = 0;  // the next copy is use number `wraps` of stage s
             int issued = 0;
             for (int u = ub; u < ue; ++u) {
+                if (wraps > 0 && !x_sent) send_x();  // before the first wait on the consumers
                 // stage s is free once every consumer warp released its previous use
                 if (wraps > 0 && !mbar_wait(&empty[s], (uint32_t)(wraps - 1) & 1u, abort_flag, &g_gemv_status)) {
                     *abort_flag = 1;
@@ -167,7 +182,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
                     ++nb;
                 }
             }
+            if (!x_sent) send_x();
             // every copy issued must land before the CTA may exit
+            (void)mbar_wait(xbar, 0, nullptr, &g_gemv_status);
             const int first = issued > S ? issued - S : 0;
             for (int i = first; i < issued; ++i) (void)mbar_wait(&full[i % S], (i / S) & 1, nullptr, &g_gemv_status);
         }
@@ -180,24 +197,23 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     const int wg = warp >> 2;              // warpgroup 0..3: takes the CTA's units i with i % 4 == wg
     const int t = (warp & 3) * 32 + lane;  // column within the tile
     const int ct = threadIdx.x;            // 0..511
-    pdl_wait();
+    bool ok = true;
+    pdl_wait();  // y and the workspace are written only after the preceding grid
     {
-        // activations to shared memory (rows m >= M zero), then per-group sums
-        const int nvec = p.M * p.K / 8;
-        const uint4* xg = reinterpret_cast<const uint4*>(p.x);
+        // rows m >= M of the activations are zero; the others come from the
+        // producer's copy; then the per-group sums
         uint4* xv = reinterpret_cast<uint4*>(xs);
-        for (int i = ct; i < M * p.K / 8; i += 32 * kGemvConsumerWarps)
-            xv[i] = i < nvec ? __ldg(xg + i) : make_uint4(0, 0, 0, 0);
+        for (int i = p.M * p.K / 8 + ct; i < M * p.K / 8; i += 32 * kGemvConsumerWarps) xv[i] = make_uint4(0, 0, 0, 0);
+        if (!mbar_wait_warp(xbar, 0, abort_flag, &g_gemv_status)) ok = false;
         consumer_bar();
-        for (int i = ct; i < M * p.KB; i += 32 * kGemvConsumerWarps) {
-            const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs) + (size_t)i * 64;  // 128 bf16
-            float a = 0.f, b = 0.f;
-#pragma unroll 8
-            for (int e = 0; e < 64; e += 2) {
-                a += bf16lo(xr[e]) + bf16hi(xr[e]);
-                b += bf16lo(xr[e + 1]) + bf16hi(xr[e + 1]);
-            }
-            xsum[i] = a + b;
+        // one group (128 values) per warp: two words per lane, then a butterfly
+        for (int i = warp; i < M * p.KB; i += kGemvConsumerWarps) {
+            const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs) + (size_t)i * 64;
+            const uint32_t v0 = xr[lane], v1 = xr[lane + 32];
+            float a = (bf16lo(v0) + bf16hi(v0)) + (bf16lo(v1) + bf16hi(v1));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+            if (lane == 0) xsum[i] = a;
         }
         consumer_bar();
     }
@@ -240,7 +256,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     fetch(sc0, zw0);
     fetch(sc1, zw1);
     uint32_t ph = 0;
-    bool ok = true;
     int u = ub;
     int nb = ub / p.KB;
     while (u < ue) {
