@@ -73,7 +73,11 @@ typedef enum {
     W4A16_EWORKSPACE = -6     /* workspace missing, too small or misaligned */
 } w4a16_status;
 
-/* Kernel choice for w4a16_gemm_path (AUTO picks per M from a measured table). */
+/*
+ * Kernel choice for w4a16_gemm_path.  AUTO picks from times measured on
+ * GB300: the GEMV when M <= 2, or M <= 4 with K*N <= 16M weights (and its
+ * activation copy fits in shared memory); the tensor-core GEMM otherwise.
+ */
 typedef enum {
     W4A16_PATH_AUTO = 0,
     W4A16_PATH_GEMV = 1,      /* CUDA-core split-K GEMV, M <= 8 */

@@ -68,11 +68,15 @@ int check_gemm(const void* x, const uint32_t* qd, const void* scales, const uint
     return W4A16_OK;
 }
 
-// Kernel choice per M.  GEMV for M <= 8 when its activation copy fits in
-// shared memory, tensor cores otherwise.
+// Kernel choice per M, from measured times on GB300 (layer shapes of a ~4B
+// decoder, M = 1..8): the GEMV's arithmetic grows with M while the
+// tensor-core kernel's time is flat in M, and they cross between M = 2 and
+// M = 4, later for smaller weight matrices.  GEMV when M <= 2, or M <= 4 with
+// at most 16M weights, and its activation copy fits in shared memory.
 int choose_path(int M, int N, int K, int sms) {
     GemvPlan gp;
-    if (M <= 8 && gemv_plan(M, N, K, sms, &gp)) return W4A16_PATH_GEMV;
+    const bool small = (long long)K * N <= (16ll << 20);
+    if ((M <= 2 || (M <= 4 && small)) && gemv_plan(M, N, K, sms, &gp)) return W4A16_PATH_GEMV;
     return W4A16_PATH_TC;
 }
 

@@ -299,3 +299,14 @@ def test_chained_layers_respect_order(M, path, flags):
         ref = oracle.gemm(x2, p2.qweight, p2.scales, p2.qzeros)
         check_close(bf16_to_f64(y2), ref, f"chain M={M} flags={flags}")
     assert w.w4a16_last_device_status() == 0
+
+
+def test_auto_path_follows_the_measured_rule():
+    """AUTO: GEMV for M <= 2, and M <= 4 when K*N <= 16M; tensor cores otherwise."""
+    import int4_weight_only_gemm_gb300 as w
+    for M, shape, want in [(1, "gate_up", w.PATH_GEMV), (2, "down", w.PATH_GEMV), (3, "qkv", w.PATH_GEMV),
+                           (4, "o_proj", w.PATH_GEMV), (3, "gate_up", w.PATH_TC), (4, "down", w.PATH_TC),
+                           (8, "qkv", w.PATH_TC), (16, "qkv", w.PATH_TC), (1, "vocab", w.PATH_GEMV),
+                           (4, "vocab", w.PATH_TC)]:
+        K, N = wi.shape_kn(shape)
+        assert w.w4a16_auto_path(M, N, K) == want, (M, shape)
