@@ -48,8 +48,10 @@ struct TcParams {
     uint32_t* counters;
     float* partials;
     int M, N, K, G;
-    int NB, MT, splits;
-    int units;       // NB * MT * splits
+    int NB, MT;
+    int whole;       // units [0, whole) are whole tiles: unit u is tile u
+    int splits;      // units from `whole` on: each later tile in `splits` K pieces
+    int units;       // whole + (tiles - whole) * splits
     int prefetch;    // weights may be loaded before the preceding grid completes
 };
 
@@ -89,17 +91,33 @@ struct TcCfg {
 };
 
 struct UnitInfo {
-    int nb, mb, split, g0, g1;
+    int nb, mb, split, ns, g0, g1;
+    int ptile;  // for a K piece (ns > 1): index of its tile among the split tiles
 };
 
+// Units: the tiles of what would be a partial last round of the persistent
+// grid, cut into K pieces spread over all CTAs, come first (so that their
+// reductions overlap the rest), then the other tiles whole.  With fewer
+// tiles than CTAs every tile is cut (whole = 0).
 __device__ __forceinline__ UnitInfo unit_info(const TcParams& p, int u) {
     UnitInfo r;
-    r.nb = u % p.NB;
-    const int rest = u / p.NB;
-    r.mb = rest % p.MT;
-    r.split = rest / p.MT;
-    r.g0 = (int)((long long)r.split * p.G / p.splits);
-    r.g1 = (int)((long long)(r.split + 1) * p.G / p.splits);
+    int tile;
+    const int pieces = p.units - p.whole;
+    if (u >= pieces) {
+        tile = u - pieces;
+        r.split = 0;
+        r.ns = 1;
+        r.ptile = -1;
+    } else {
+        r.ptile = u / p.splits;
+        r.split = u - r.ptile * p.splits;
+        r.ns = p.splits;
+        tile = p.whole + r.ptile;
+    }
+    r.nb = tile % p.NB;
+    r.mb = tile / p.NB;
+    r.g0 = (int)((long long)r.split * p.G / r.ns);
+    r.g1 = (int)((long long)(r.split + 1) * p.G / r.ns);
     return r;
 }
 
@@ -407,7 +425,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
             const int n = 128 * ui.nb + t;
             const int tok0 = ui.mb * NT + r * CW;
             if (all_ok) {
-                if (p.splits == 1) {
+                if (ui.ns == 1) {
                     if (t < W) {
 #pragma unroll
                         for (int j = 0; j < CW; ++j)
@@ -416,9 +434,9 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                                     f32_to_bf16_rn((j & 1) ? acc[j / 2].y : acc[j / 2].x);
                     }
                 } else {
-                    const int tile = ui.mb * p.NB + ui.nb;
-                    // partial sums: [tile][split][column t][NT tokens], this warpgroup's CW tokens
-                    float4* part = reinterpret_cast<float4*>(p.partials + (((size_t)tile * p.splits + ui.split) * 128 + t) * NT + r * CW);
+                    const int tile = ui.ptile;  // counters and partials of the split tiles only
+                    // partial sums: [split tile][piece][column t][NT tokens], this warpgroup's CW tokens
+                    float4* part = reinterpret_cast<float4*>(p.partials + (((size_t)tile * ui.ns + ui.split) * 128 + t) * NT + r * CW);
 #pragma unroll
                     for (int j = 0; j < CW; j += 4)
                         part[j / 4] = make_float4(acc[j / 2].x, acc[j / 2].y, acc[j / 2 + 1].x, acc[j / 2 + 1].y);
@@ -430,7 +448,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                     if (rt == 0) {
                         __threadfence();
                         const unsigned old = atomicAdd(&p.counters[tile], 1u);
-                        const int last = old == (unsigned)p.splits - 1;
+                        const int last = old == (unsigned)ui.ns - 1;
                         if (last) __threadfence();
                         *sh_last = last;
                     }
@@ -438,7 +456,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                     if (*sh_last) {
                         // every split's values for this thread, summed in split order,
                         // 16 tokens at a time
-                        const float4* base = reinterpret_cast<const float4*>(p.partials + ((size_t)tile * p.splits * 128 + t) * NT + r * CW);
+                        const float4* base = reinterpret_cast<const float4*>(p.partials + ((size_t)tile * ui.ns * 128 + t) * NT + r * CW);
                         const size_t sstride = (size_t)128 * NT / 4;  // float4s between splits
 #pragma unroll 1
                         for (int j0 = 0; j0 < CW; j0 += 16) {
@@ -446,7 +464,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
 #pragma unroll
                             for (int j = 0; j < 4; ++j) sum[j] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-                            for (int sp = 0; sp < p.splits; ++sp) {
+                            for (int sp = 0; sp < ui.ns; ++sp) {
 #pragma unroll
                                 for (int j = 0; j < 4; ++j) {
                                     const float4 v = __ldcg(base + sp * sstride + j0 / 4 + j);
@@ -497,25 +515,51 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
     const int MT = (M + NT - 1) / NT;
     const long long slots = sms;  // one CTA per SM
     const long long tiles = (long long)L.NB * MT;
-    // Split K when there are fewer tiles than SMs (at least 2 groups a split),
-    // rounding down: every CTA then runs at most one unit, so no SM does twice
-    // the work of the others while most idle.
+    const int max_split = G / 2 > 0 ? G / 2 : 1;  // at least 2 groups a piece
+    long long whole = tiles;
+    // Pieces of a partial last round only for long K (at least 48 groups),
+    // at least 8 groups each: measured at M = 2048, cutting the tail of
+    // 9728-deep tiles saved 8 % while cutting 2560- and 4096-deep tiles
+    // (pieces of 4 to 10 groups) cost 10 %, the pieces' reduction
+    // outweighing the balance.
+    const int max_split_tail = G >= 48 ? G / 8 : 1;
     int splits = 1;
     if (tiles < slots) {
-        splits = (int)(slots / tiles);
-        const int max_split = G / 2 > 0 ? G / 2 : 1;
-        if (splits > max_split) splits = max_split;
+        // Fewer tiles than CTAs: every tile in K pieces, rounded down so that
+        // no CTA runs two units while others idle.
+        const long long s = slots / tiles < max_split ? slots / tiles : max_split;
+        if (s > 1) {
+            splits = (int)s;
+            whole = 0;
+        }
+    } else if (tiles % slots) {
+        // Full rounds of whole tiles; the tiles of the partial last round in
+        // K pieces spread over all CTAs.
+        const long long rem = tiles % slots;
+        const long long s = slots / rem < max_split_tail ? slots / rem : max_split_tail;
+        if (s > 1) {
+            splits = (int)s;
+            whole = tiles - rem;
+        }
     }
-    if (splits > 1 && (size_t)tiles > kMaxCounters) splits = 1;
-    const long long units = tiles * splits;
+    if (tiles - whole > (long long)kMaxCounters) {  // counters for the split tiles
+        whole = tiles;
+        splits = 1;
+    }
+    const long long units = whole + (tiles - whole) * splits;
     if (units >= (1ll << 31)) return false;
     out->NT = NT;
     out->MT = MT;
     out->NB = L.NB;
+    out->whole = (int)whole;
     out->splits = splits;
+    out->units = (int)units;
     out->ctas = (int)(units < slots ? units : slots);
     out->smem = NT == 16 ? TcCfg<16>::kAlloc : NT == 32 ? TcCfg<32>::kAlloc : TcCfg<128>::kAlloc;
-    out->ws_bytes = splits > 1 ? ws_counter_bytes(tiles) + (size_t)tiles * splits * NT * 128 * sizeof(float) : 0;
+    const long long split_tiles = tiles - whole;
+    out->ws_bytes = split_tiles > 0
+                        ? ws_counter_bytes((size_t)split_tiles) + (size_t)split_tiles * splits * NT * 128 * sizeof(float)
+                        : 0;
     return true;
 }
 
@@ -572,17 +616,18 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
     prm.scales = scales;
     prm.qzeros = qzeros;
     prm.y = y;
-    const size_t tiles = (size_t)plan.NB * plan.MT;
+    const size_t split_tiles = (size_t)plan.NB * plan.MT - (size_t)plan.whole;
     prm.counters = reinterpret_cast<uint32_t*>(ws);
-    prm.partials = ws ? reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + ws_counter_bytes(tiles)) : nullptr;
+    prm.partials = ws ? reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + ws_counter_bytes(split_tiles)) : nullptr;
     prm.M = M;
     prm.N = N;
     prm.K = K;
     prm.G = K / 128;
     prm.NB = plan.NB;
     prm.MT = plan.MT;
+    prm.whole = plan.whole;
     prm.splits = plan.splits;
-    prm.units = plan.NB * plan.MT * plan.splits;
+    prm.units = plan.units;
     const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     switch (plan.NT) {

@@ -28,7 +28,9 @@ int gemv_read_status();
 
 // tcgen05 tensor-core GEMM (any M)
 struct TcPlan {
-    int NT, MT, NB, splits;  // tokens per tile, token tiles, column tiles, K splits
+    int NT, MT, NB;          // tokens per tile, token tiles, column tiles
+    int whole, splits;       // tiles [0, whole) whole, the rest in `splits` K pieces each
+    int units;               // whole + (NB * MT - whole) * splits
     int ctas;                // persistent CTAs
     size_t smem, ws_bytes;
 };
