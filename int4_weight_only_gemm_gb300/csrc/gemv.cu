@@ -14,13 +14,15 @@
 // piece: every CTA then streams about the same number of bytes and ends with
 // exactly one tile segment, so no CTA stops mid-stream to hand on a tile.
 //
-// Data movement: a producer warp copies the packed weights of whole units
-// into a ring of shared-memory stages, one bulk asynchronous copy per unit
-// (mbarrier transaction counts), as far ahead as the ring allows, so a CTA
-// has most of its bytes requested at once and the loads never wait on the
-// arithmetic.  The copy engine keeps only a few copies in flight per SM, so
-// a unit is one copy: each thread loads its column's fp16 scale and zero
-// word itself, two units ahead of use.
+// Data movement: a producer warp copies the packed weights into a ring of
+// shared-memory stages of two consecutive units (16 KB, contiguous in the
+// device layout: one bulk asynchronous copy, mbarrier transaction counts),
+// as far ahead as the ring allows, so a CTA has most of its bytes requested
+// at once and the loads never wait on the arithmetic.  The copy engine
+// spends about the same time on every copy, whatever its size, so the
+// copies are large: 16 KB ones stream 4.9 TB/s on this GPU, 8 KB ones 4.5.
+// Each thread loads its column's fp16 scale and zero word itself, two units
+// ahead of use.
 //
 // Arithmetic: four consumer warpgroups take the CTA's units in turn (unit i
 // goes to warpgroup i % 4), thread t column t: four 128-bit shared loads give
@@ -61,8 +63,9 @@ struct GemvParams {
 
 constexpr int kGemvConsumerWarps = 16;                       // four warpgroups
 constexpr int kGemvThreads = 32 * (kGemvConsumerWarps + 1);  // plus the producer warp
-constexpr int kGemvStage = 8192;                             // packed weights of one unit, W * 64 bytes
-constexpr int kGemvMaxStages = 32;
+constexpr int kGemvUnit = 8192;                              // packed weights of one unit, W * 64 bytes
+constexpr int kGemvStage = 2 * kGemvUnit;                    // a stage: two units, the second at 8 KB
+constexpr int kGemvMaxStages = 16;
 constexpr int kGemvMaxSmem = 226 * 1024;
 
 // Pieces of tile t, and the first CTA of tile t (split mode).
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
         mbar_init(&full[threadIdx.x], 1);  // the producer's expect-tx arrival
         fence_mbar_init();
     } else if (threadIdx.x >= 32 && threadIdx.x < 32 + S) {
-        mbar_init(&empty[threadIdx.x - 32], 4);  // one arrival per warp of the consuming warpgroup
+        mbar_init(&empty[threadIdx.x - 32], 8);  // one arrival per warp of the two consuming warpgroups
         fence_mbar_init();
     }
     if (threadIdx.x == 64) {
@@ -160,25 +163,40 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
             };
             if (!p.prefetch) send_x();
             int nb = ub / p.KB, kb = ub - nb * p.KB;
-            int s = 0, wraps = 0;  // the next copy is use number `wraps` of stage s
+            int s = 0, wraps = 0;  // the next stage is use number `wraps` of stage s
             int issued = 0;
-            for (int u = ub; u < ue; ++u) {
+            for (int u = ub; u < ue; u += 2) {
                 if (wraps > 0 && !x_sent) send_x();  // before the first wait on the consumers
                 // stage s is free once every consumer warp released its previous use
                 if (wraps > 0 && !mbar_wait(&empty[s], (uint32_t)(wraps - 1) & 1u, abort_flag, &g_gemv_status)) {
                     *abort_flag = 1;
                     break;
                 }
-                const int W = L.width(nb);
-                mbar_arrive_expect_tx(&full[s], (uint32_t)W * 64);
-                bulk_g2s(ring + (size_t)s * kGemvStage, p.qd + L.block_word(nb, kb), (uint32_t)W * 64, &full[s]);
+                const int W0 = L.width(nb);
+                const bool two = u + 1 < ue;
+                const int nb1 = kb + 1 < p.KB ? nb : nb + 1;  // the second unit's tile
+                const int W1 = two ? L.width(nb1) : 0;
+                unsigned char* st = ring + (size_t)s * kGemvStage;
+                const uint32_t* src = p.qd + L.block_word(nb, kb);
+                mbar_arrive_expect_tx(&full[s], (uint32_t)(W0 + W1) * 64);
+                if (W0 == 128) {
+                    // a full first unit: the second follows it in memory (same tile,
+                    // or the next one), one copy lands both
+                    bulk_g2s(st, src, (uint32_t)(W0 + W1) * 64, &full[s]);
+                } else {
+                    // a ragged first unit (the last tile): the second, if any, is
+                    // ragged too and goes to the stage's second half
+                    bulk_g2s(st, src, (uint32_t)W0 * 64, &full[s]);
+                    if (two) bulk_g2s(st + kGemvUnit, src + W0 * 16, (uint32_t)W1 * 64, &full[s]);
+                }
                 ++issued;
                 if (++s == S) {
                     s = 0;
                     ++wraps;
                 }
-                if (++kb == p.KB) {
-                    kb = 0;
+                kb += 2;
+                while (kb >= p.KB) {
+                    kb -= p.KB;
                     ++nb;
                 }
             }
@@ -230,8 +248,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     // independent accumulation chains per 32-row chunk and token: one per
     // word for few tokens, one per chunk when the tokens already give the ILP
     constexpr int NCH = M <= 2 ? 4 : 1;
-    int i = wg;  // this warpgroup's next unit, relative to the CTA's first
-    int s = wg;  // its stage (S >= 4)
+    int i = wg;       // this warpgroup's next unit, relative to the CTA's first
+    int s = wg >> 1;  // its stage (unit i is in stage i / 2 of the walk; S >= 2)
+    const uint32_t half = (uint32_t)(wg & 1) * kGemvUnit;  // and in that stage's half i % 2
     // scale and zero word of this thread's column for the warpgroup's units,
     // loaded two units ahead of use: (sc0, zw0) for unit i, (sc1, zw1) for i + 4
     int pv = ub + wg;  // next unit to fetch
@@ -272,7 +291,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
         for (int m = 0; m < M; ++m) acc[m] = 0.f;
         for (; ub + i < seg_end; i += 4) {
             const int kb = ub + i - t0u;
-            const uint32_t st_a = ring_a + (uint32_t)s * kGemvStage;
+            const uint32_t st_a = ring_a + (uint32_t)s * kGemvStage + half;
             if (ok) {
                 const bool ready = mbar_try_wait(full_a + 8u * (uint32_t)s, ph);
                 if (!__all_sync(0xFFFFFFFFu, ready) &&
@@ -331,7 +350,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
             fetch(sc1, zw1);
             // this warp is done with the stage (its shared loads have returned)
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty_a + 8u * (uint32_t)s) : "memory");
-            s += 4;
+            s += 2;  // the warpgroup's next unit, four on, is two stages on
             if (s >= S) {
                 s -= S;
                 ph ^= 1;
@@ -432,11 +451,11 @@ bool gemv_plan(int M, int N, int K, int sms, GemvPlan* out) {
     }
     const size_t fixed = GemvSmem(MT, K, 0).total;
     const size_t per_stage = kGemvStage + 16;
-    if (fixed + 4 * per_stage > (size_t)kGemvMaxSmem) return false;
+    if (fixed + 2 * per_stage > (size_t)kGemvMaxSmem) return false;
     long long S = (long long)(((size_t)kGemvMaxSmem - fixed) / per_stage);
     if (S > kGemvMaxStages) S = kGemvMaxStages;
-    if (S > per) S = per;
-    if (S < 4) S = 4;  // four warpgroups each hold a stage
+    if (S > (per + 1) / 2) S = (per + 1) / 2;
+    if (S < 2) S = 2;  // the two pairs of warpgroups each hold a stage
     if (fixed + (size_t)S * per_stage > (size_t)kGemvMaxSmem) return false;
     const GemvSmem lay(MT, K, (int)S);
     if (lay.xsum % 16 || lay.red % 16 || lay.bars % 16) return false;  // never: regions are rounded up
