@@ -15,12 +15,13 @@
 // exactly one tile segment, so no CTA stops mid-stream to hand on a tile.
 //
 // Data movement: a producer warp copies the packed weights into a ring of
-// shared-memory stages of two consecutive units (16 KB, contiguous in the
+// shared-memory stages of four consecutive units (32 KB, contiguous in the
 // device layout: one bulk asynchronous copy, mbarrier transaction counts),
 // as far ahead as the ring allows, so a CTA has most of its bytes requested
 // at once and the loads never wait on the arithmetic.  The copy engine
 // spends about the same time on every copy, whatever its size, so the
-// copies are large: 16 KB ones stream 4.9 TB/s on this GPU, 8 KB ones 4.5.
+// copies are large (on this GPU a ring of 8 KB copies streams 4.5 TB/s,
+// of 16 KB or larger ones 4.9 TB/s).
 // Each thread loads its column's fp16 scale and zero word itself, two units
 // ahead of use.
 //
@@ -64,8 +65,9 @@ struct GemvParams {
 constexpr int kGemvConsumerWarps = 16;                       // four warpgroups
 constexpr int kGemvThreads = 32 * (kGemvConsumerWarps + 1);  // plus the producer warp
 constexpr int kGemvUnit = 8192;                              // packed weights of one unit, W * 64 bytes
-constexpr int kGemvStage = 2 * kGemvUnit;                    // a stage: two units, the second at 8 KB
-constexpr int kGemvMaxStages = 16;
+constexpr int kStageUnits = 4;                               // units per stage: one per warpgroup
+constexpr int kGemvStage = kStageUnits * kGemvUnit;          // unit j of a stage at j * 8 KB
+constexpr int kGemvMaxStages = 8;
 constexpr int kGemvMaxSmem = 226 * 1024;
 
 // Pieces of tile t, and the first CTA of tile t (split mode).
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
         mbar_init(&full[threadIdx.x], 1);  // the producer's expect-tx arrival
         fence_mbar_init();
     } else if (threadIdx.x >= 32 && threadIdx.x < 32 + S) {
-        mbar_init(&empty[threadIdx.x - 32], 8);  // one arrival per warp of the two consuming warpgroups
+        mbar_init(&empty[threadIdx.x - 32], 16);  // one arrival per consumer warp
         fence_mbar_init();
     }
     if (threadIdx.x == 64) {
@@ -165,39 +167,49 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
             int nb = ub / p.KB, kb = ub - nb * p.KB;
             int s = 0, wraps = 0;  // the next stage is use number `wraps` of stage s
             int issued = 0;
-            for (int u = ub; u < ue; u += 2) {
+            for (int u = ub; u < ue; u += kStageUnits) {
                 if (wraps > 0 && !x_sent) send_x();  // before the first wait on the consumers
                 // stage s is free once every consumer warp released its previous use
                 if (wraps > 0 && !mbar_wait(&empty[s], (uint32_t)(wraps - 1) & 1u, abort_flag, &g_gemv_status)) {
                     *abort_flag = 1;
                     break;
                 }
-                const int W0 = L.width(nb);
-                const bool two = u + 1 < ue;
-                const int nb1 = kb + 1 < p.KB ? nb : nb + 1;  // the second unit's tile
-                const int W1 = two ? L.width(nb1) : 0;
+                const int n = ue - u < kStageUnits ? ue - u : kStageUnits;
                 unsigned char* st = ring + (size_t)s * kGemvStage;
-                const uint32_t* src = p.qd + L.block_word(nb, kb);
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(W0 + W1) * 64);
-                if (W0 == 128) {
-                    // a full first unit: the second follows it in memory (same tile,
-                    // or the next one), one copy lands both
-                    bulk_g2s(st, src, (uint32_t)(W0 + W1) * 64, &full[s]);
-                } else {
-                    // a ragged first unit (the last tile): the second, if any, is
-                    // ragged too and goes to the stage's second half
-                    bulk_g2s(st, src, (uint32_t)W0 * 64, &full[s]);
-                    if (two) bulk_g2s(st + kGemvUnit, src + W0 * 16, (uint32_t)W1 * 64, &full[s]);
+                // bytes first (the expected transaction count), then the copies:
+                // a run of full-width units is contiguous in memory and lands
+                // with one copy; a unit of the ragged last tile has its own
+                uint32_t bytes = 0;
+                {
+                    int tnb = nb, tkb = kb;
+                    for (int j = 0; j < n; ++j) {
+                        bytes += (uint32_t)L.width(tnb) * 64;
+                        if (++tkb == p.KB) { tkb = 0; ++tnb; }
+                    }
+                }
+                mbar_arrive_expect_tx(&full[s], bytes);
+                int j = 0;
+                while (j < n) {
+                    const int W = L.width(nb);
+                    const uint32_t* src = p.qd + L.block_word(nb, kb);
+                    int run = 1;
+                    if (W == 128) {  // following units of full tiles (this tile or the next ones)
+                        int tnb = nb, tkb = kb;
+                        while (j + run < n) {
+                            if (++tkb == p.KB) { tkb = 0; ++tnb; }
+                            if (L.width(tnb) != 128) break;
+                            ++run;
+                        }
+                    }
+                    bulk_g2s(st + (size_t)j * kGemvUnit, src, (uint32_t)(run * W) * 64, &full[s]);
+                    j += run;
+                    for (int k = 0; k < run; ++k)
+                        if (++kb == p.KB) { kb = 0; ++nb; }
                 }
                 ++issued;
                 if (++s == S) {
                     s = 0;
                     ++wraps;
-                }
-                kb += 2;
-                while (kb >= p.KB) {
-                    kb -= p.KB;
-                    ++nb;
                 }
             }
             if (!x_sent) send_x();
@@ -248,9 +260,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     // independent accumulation chains per 32-row chunk and token: one per
     // word for few tokens, one per chunk when the tokens already give the ILP
     constexpr int NCH = M <= 2 ? 4 : 1;
-    int i = wg;       // this warpgroup's next unit, relative to the CTA's first
-    int s = wg >> 1;  // its stage (unit i is in stage i / 2 of the walk; S >= 2)
-    const uint32_t half = (uint32_t)(wg & 1) * kGemvUnit;  // and in that stage's half i % 2
+    int i = wg;  // this warpgroup's next unit, relative to the CTA's first
+    int s = 0;   // its stage: unit i is unit i % 4 of stage i / 4 of the walk
+    const uint32_t half = (uint32_t)wg * kGemvUnit;
     // scale and zero word of this thread's column for the warpgroup's units,
     // loaded two units ahead of use: (sc0, zw0) for unit i, (sc1, zw1) for i + 4
     int pv = ub + wg;  // next unit to fetch
@@ -350,9 +362,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
             fetch(sc1, zw1);
             // this warp is done with the stage (its shared loads have returned)
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty_a + 8u * (uint32_t)s) : "memory");
-            s += 2;  // the warpgroup's next unit, four on, is two stages on
-            if (s >= S) {
-                s -= S;
+            if (++s == S) {  // the warpgroup's next unit, four on, is in the next stage
+                s = 0;
                 ph ^= 1;
             }
         }
@@ -451,12 +462,12 @@ bool gemv_plan(int M, int N, int K, int sms, GemvPlan* out) {
     }
     const size_t fixed = GemvSmem(MT, K, 0).total;
     const size_t per_stage = kGemvStage + 16;
-    if (fixed + 2 * per_stage > (size_t)kGemvMaxSmem) return false;
+    if (fixed + per_stage > (size_t)kGemvMaxSmem) return false;
     long long S = (long long)(((size_t)kGemvMaxSmem - fixed) / per_stage);
     if (S > kGemvMaxStages) S = kGemvMaxStages;
-    if (S > (per + 1) / 2) S = (per + 1) / 2;
-    if (S < 2) S = 2;  // the two pairs of warpgroups each hold a stage
-    if (fixed + (size_t)S * per_stage > (size_t)kGemvMaxSmem) return false;
+    long long want = (per + kStageUnits - 1) / kStageUnits;  // stages a CTA uses
+    if (want < 2) want = 2;  // one stage filling while another is consumed
+    if (S > want) S = want;  // (one stage when no more fits: correct, without overlap)
     const GemvSmem lay(MT, K, (int)S);
     if (lay.xsum % 16 || lay.red % 16 || lay.bars % 16) return false;  // never: regions are rounded up
     out->ctas = ctas;
