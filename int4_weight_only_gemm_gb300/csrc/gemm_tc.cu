@@ -116,8 +116,9 @@ __device__ __forceinline__ UnitInfo unit_info(const TcParams& p, int u) {
     }
     r.nb = tile % p.NB;
     r.mb = tile / p.NB;
-    r.g0 = (int)((long long)r.split * p.G / r.ns);
-    r.g1 = (int)((long long)(r.split + 1) * p.G / r.ns);
+    // unsigned 32-bit: split < ns <= CTAs (< 256) and G < 2^24, so no overflow
+    r.g0 = (int)((unsigned)r.split * (unsigned)p.G / (unsigned)r.ns);
+    r.g1 = (int)((unsigned)(r.split + 1) * (unsigned)p.G / (unsigned)r.ns);
     return r;
 }
 
@@ -157,14 +158,18 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
     const int lane = threadIdx.x & 31;
     const Layout L(p.K, p.N);
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < SS; ++i) mbar_init(&full[i], 2);  // one arrival per producer warp
-        for (int i = 0; i < ND; ++i) mbar_init(&done[i], 1);
-        for (int i = 0; i < SA; ++i) mbar_init(&a_full[i], 4);
-        for (int i = 0; i < C::NDB; ++i) mbar_init(&d_empty[i], 4 * R);
-        mbar_init(mma_done, 1);
-        *abort_flag = 0;
-        fence_mbar_init();
+    // barriers initialised in parallel, one per thread
+    {
+        const int i = threadIdx.x;
+        if (i < SS) mbar_init(&full[i], 2);  // one arrival per producer warp
+        else if (i < SS + ND) mbar_init(&done[i - SS], 1);
+        else if (i < SS + ND + SA) mbar_init(&a_full[i - SS - ND], 4);
+        else if (i < SS + ND + SA + C::NDB) mbar_init(&d_empty[i - SS - ND - SA], 4 * R);
+        else if (i == SS + ND + SA + C::NDB) {
+            mbar_init(mma_done, 1);
+            *abort_flag = 0;
+        }
+        if (i <= SS + ND + SA + C::NDB) fence_mbar_init();
     }
     if (warp == C::kProdWarp) {
         tmem_alloc(tmem_holder, C::kTmemCols);
