@@ -296,22 +296,39 @@ def time_graph_steps(torch, per_step, rot, copies, steps, warmup, barrier=None):
 
 
 def measure_e2e(w, torch, wl, steps):
-    """Through the public binding with host buffers: per step, pinned-host
-    activations go to the device, the four GEMMs run, the outputs come back to
-    pinned host memory, and the host waits for them."""
-    hx = [g["x"].cpu().pin_memory() for g in wl.gemms]
-    hy = [torch.empty_like(g["y"], device="cpu").pin_memory() for g in wl.gemms]
-    dx = [torch.empty_like(g["x"]) for g in wl.gemms]
-    h2d = sum(t.numel() * 2 for t in hx)
-    d2h = sum(t.numel() * 2 for t in hy)
+    """Through the public binding with host buffers: per step, the step's
+    activations (one pinned host buffer holding the four GEMMs' inputs) go to
+    the device in one copy, the four GEMMs run, their outputs (one device
+    buffer) come back to pinned host memory in one copy, and the host waits."""
+    xs = [g["x"] for g in wl.gemms]
+    ys = [g["y"] for g in wl.gemms]
+    xn = [t.numel() for t in xs]
+    yn = [t.numel() for t in ys]
+    # 16-byte aligned slices (8 bf16) of one buffer per direction
+    xo = [0]
+    for n in xn:
+        xo.append(xo[-1] + (n + 7) // 8 * 8)
+    yo = [0]
+    for n in yn:
+        yo.append(yo[-1] + (n + 7) // 8 * 8)
+    hx = torch.zeros(xo[-1], dtype=torch.bfloat16).pin_memory()
+    for j, t in enumerate(xs):
+        hx[xo[j]:xo[j] + xn[j]].copy_(t.reshape(-1).cpu())
+    hy = torch.empty(yo[-1], dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty(xo[-1], dtype=torch.bfloat16, device=xs[0].device)
+    dy = torch.empty(yo[-1], dtype=torch.bfloat16, device=xs[0].device)
+    dxs = [dx[xo[j]:xo[j] + xn[j]].view(xs[j].shape) for j in range(len(xs))]
+    dys = [dy[yo[j]:yo[j] + yn[j]].view(ys[j].shape) for j in range(len(ys))]
+    h2d = hx.numel() * 2
+    d2h = hy.numel() * 2
     stream = torch.cuda.current_stream()
 
     def one(i):
         c = i % wl.copies
+        dx.copy_(hx, non_blocking=True)
         for j, g in enumerate(wl.gemms):
-            dx[j].copy_(hx[j], non_blocking=True)
-            w.w4a16_gemm(dx[j], g["qds"][c], g["sc"], g["qz"], out=g["y"], workspace=g["ws"])
-            hy[j].copy_(g["y"], non_blocking=True)
+            w.w4a16_gemm(dxs[j], g["qds"][c], g["sc"], g["qz"], out=dys[j], workspace=g["ws"])
+        hy.copy_(dy, non_blocking=True)
         stream.synchronize()
 
     for i in range(min(20, steps)):
