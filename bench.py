@@ -340,22 +340,31 @@ def measure_e2e(w, torch, wl, steps):
     return wl.bytes * steps / dt / 1e9, h2d, d2h, dt / steps * 1e3
 
 
-def cpu_baseline(min_seconds=8.0):
+def cpu_baseline(min_seconds=8.0, one_core_seconds=3.0):
+    """The oracle on the host cores: all of them (OpenMP default), then one."""
     import oracle
     _, seed, items = wi.CONFIGS[1]
     probs = [wi.generate_named(s, M, seed) for (s, M) in items]
     step_bytes = sum(gemm_bytes(p.M, p.K, p.N) for p in probs)
-    n = 0
-    t0 = time.perf_counter()
-    while True:
-        for p in probs:
-            oracle.gemm(p.x, p.qweight, p.scales, p.qzeros)
-        n += 1
-        dt = time.perf_counter() - t0
-        if dt >= min_seconds or n >= 200:
-            break
-    return {"value": step_bytes * n / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"the full decode set (4 projections, M=1) repeated {n} times, {dt:.1f} s"}
+    cores = oracle.max_threads()
+
+    def timed(limit, nthreads):
+        n = 0
+        t0 = time.perf_counter()
+        while True:
+            for p in probs:
+                oracle.gemm(p.x, p.qweight, p.scales, p.qzeros, nthreads=nthreads)
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= limit or n >= 200:
+                return n, dt
+
+    n, dt = timed(min_seconds, 0)
+    n1, dt1 = timed(one_core_seconds, 1)  # last: the thread count set here persists
+    return {"value": step_bytes * n / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"the full decode set (4 projections, M=1) repeated {n} times, {dt:.1f} s",
+            "one_core": {"value": step_bytes * n1 / dt1 / 1e9, "cores": 1,
+                         "sample": f"the same set repeated {n1} times, {dt1:.1f} s"}}
 
 
 def run_case(case, reps):
