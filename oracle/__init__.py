@@ -230,3 +230,32 @@ def gemm_numpy(x, qweight, scales, qzeros, group: int = 128) -> np.ndarray:
     gidx = np.arange(K) // group
     W = (q - z[gidx].astype(np.float64)) * s[gidx]
     return np.matmul(_np_bf16(x), W)
+
+
+def requant_codes(w, scales, qzeros, group: int = 128) -> np.ndarray:
+    """Grid-preserving re-quantization: codes[k][n] = clamp(round(w / s) + z, 0, 15).
+
+    The packing step of "Quantize the Target, Quantize the Drafter" (pith.science
+    review, "Assumptions & free parameters": packing rounds the updated bf16
+    weights back onto the frozen per-group scales; referee report summary: the
+    model is re-packed onto the same grid).  w[K][N] are bf16 bits, scales
+    [K/g][N] fp16 bits, qzeros [K/g][N/8] as for the GEMM; returns uint8 codes.
+
+    The pages fix neither the rounding rule nor the precision of the quotient.
+    Readings: round half to even, and the decision taken in IEEE binary32 --
+    w and s are exact in binary32, w / s is the correctly rounded binary32
+    quotient, rounded to the nearest integer (ties to even), z added, and the
+    sum clipped to 0..15 -- the precision the CUDA kernel computes in.
+    """
+    w = np.asarray(w, dtype=np.uint16)
+    K, N = w.shape
+    G = K // group
+    wf = bf16_to_f64(w).astype(np.float32)                       # exact
+    sf = f16_to_f64(np.asarray(scales, dtype=np.uint16)).astype(np.float32)  # exact
+    z = unpack_zeros(np.asarray(qzeros, dtype=np.uint32)).astype(np.float32)  # [G][N]
+    gi = np.arange(K) // group                                   # group of row k
+    quot = (wf / sf[gi, :]).astype(np.float32)                   # IEEE binary32 division
+    r = np.rint(quot)                                            # nearest integer, ties to even
+    c = np.clip(r + z[gi, :], 0.0, 15.0)
+    assert c.shape == (K, N) and G * group == K
+    return c.astype(np.uint8)
