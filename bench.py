@@ -367,6 +367,33 @@ def cpu_baseline(min_seconds=8.0, one_core_seconds=3.0):
                          "sample": f"the same set repeated {n1} times, {dt1:.1f} s"}}
 
 
+def measure_requant(w, torch, device, hbm, reps=200):
+    """Grid-preserving re-quantization of the gate_up weights (2560 x 19456)
+    straight into the device layout, two weight copies alternating (> L2)."""
+    K, N = wi.shape_kn("gate_up")
+    p = wi.generate(1, K, N, seed=5, shape_index=2)
+    ws = [torch.from_numpy(wi.random_weights(K, N, seed=5 + i).view(np.int16)).to(device).view(torch.bfloat16)
+          for i in range(2)]
+    sc = torch.from_numpy(p.scales.view(np.int16)).to(device).view(torch.float16)
+    qz = torch.from_numpy(p.qzeros.view(np.int32)).to(device)
+    outs = [torch.empty((K // 8, N), dtype=torch.int32, device=device) for _ in range(2)]
+    for i in range(10):
+        w.w4a16_requant_pack(ws[i % 2], sc, qz, out=outs[i % 2])
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(reps):
+        w.w4a16_requant_pack(ws[i % 2], sc, qz, out=outs[i % 2])
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    G = K // 128
+    nbytes = K * N * 2 + G * N * 2 + G * N // 2 + K * N // 2
+    return {"us": us, "GB/s": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / hbm,
+            "bytes": nbytes, "shape": f"{K}x{N}", "launch": "stream loop of launches (no graph)"}
+
+
 def run_case(case, reps):
     """One seeded GEMM of the named layer shape, launched `reps` times back to
     back on the current stream (the workload of the ncu summaries)."""
@@ -496,6 +523,9 @@ def main():
                            "workload": ", ".join(f"{s} M={M}" for s, M in items), "per_gemm": per2}
             del wl2, ps, rt
             torch.cuda.empty_cache()
+
+    if rank == 0 and not args.no_extra:
+        extra["requant_pack_gate_up"] = measure_requant(w, torch, device, hbm)
 
     e2e = None
     if not args.no_e2e:

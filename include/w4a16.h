@@ -98,6 +98,34 @@ int w4a16_unpack(const uint32_t *qweight_dev, uint32_t *qweight, int K, int N,
                  w4a16_stream_t stream);
 
 /*
+ * Grid-preserving re-quantization into the device layout ("Quantize the
+ * Target, Quantize the Drafter", pith.science review, "Assumptions & free
+ * parameters": packing rounds the updated bf16 weights back onto the frozen
+ * per-group scales; referee report summary: re-packed onto the same grid):
+ *
+ *     code[k][n] = clamp(round(w[k][n] / s[k/128][n]) + z[k/128][n], 0, 15)
+ *
+ * decided in IEEE binary32: the correctly rounded quotient, rounded to the
+ * nearest integer with ties to even, then z added and the sum clipped.  The
+ * codes are written in the device layout documented above (the same words
+ * w4a16_pack makes from canonical codes), ready for w4a16_gemm with the same
+ * scales and qzeros.
+ *
+ *   w            bf16 [K][N] row-major, device
+ *   scales       fp16 [K/group][N], device (the frozen grid)
+ *   qzeros       u32 [K/group][N/8], device, nibble n%8 of word n/8
+ *   qweight_dev  u32 [K/8][N] words, device, written completely
+ *
+ * All four 16-byte aligned (W4A16_EALIGN); group must be 128
+ * (W4A16_EUNSUPPORTED), K % 128 == 0 and K <= 2 097 024, N % 8 == 0
+ * (W4A16_EINVAL / W4A16_EUNSUPPORTED); qweight_dev may not overlap the inputs
+ * (W4A16_EINVAL).  Asynchronous on `stream`; the caller owns every buffer.
+ * Non-finite w or s give unspecified codes.
+ */
+int w4a16_requant_pack(const void *w, const void *scales, const uint32_t *qzeros, int K, int N,
+                       int group, uint32_t *qweight_dev, w4a16_stream_t stream);
+
+/*
  * Bytes of workspace w4a16_gemm needs for this problem on the current device
  * (0 when the chosen plan needs none).  Returns 0 for invalid arguments too.
  * The workspace carries per-tile arrival counters (its first 64 KB) and

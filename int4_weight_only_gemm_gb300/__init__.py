@@ -57,6 +57,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib = ctypes.CDLL(path)
             vp, sz, ci = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
             lib.w4a16_pack.argtypes = [vp, vp, ci, ci, vp]
+            lib.w4a16_requant_pack.argtypes = [vp, vp, vp, ci, ci, ci, vp, vp]
             lib.w4a16_unpack.argtypes = [vp, vp, ci, ci, vp]
             lib.w4a16_workspace_bytes.argtypes = [ci, ci, ci, ci]
             lib.w4a16_workspace_bytes.restype = sz
@@ -112,6 +113,25 @@ def w4a16_pack(qweight: torch.Tensor, out: torch.Tensor | None = None, stream=No
         out = torch.empty_like(qweight)
     _check(out, "out", torch.int32, qweight.shape)
     _raise(load_library().w4a16_pack(qweight.data_ptr(), out.data_ptr(), K, N, _stream(stream)), "w4a16_pack")
+    return out
+
+
+def w4a16_requant_pack(w: torch.Tensor, scales: torch.Tensor, qzeros: torch.Tensor, group: int = 128,
+                       out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Re-quantize bf16 w [K, N] onto the frozen grid (scales, qzeros) straight
+    into the device layout: code = clamp(round(w / s) + z, 0, 15)."""
+    _check(w, "w", torch.bfloat16)
+    if w.dim() != 2:
+        raise ValueError("w must be [K, N]")
+    K, N = w.shape
+    G = K // group
+    _check(scales, "scales", torch.float16, (G, N))
+    _check(qzeros, "qzeros", torch.int32, (G, N // 8))
+    if out is None:
+        out = torch.empty((K // 8, N), dtype=torch.int32, device=w.device)
+    _check(out, "out", torch.int32, (K // 8, N))
+    _raise(load_library().w4a16_requant_pack(w.data_ptr(), scales.data_ptr(), qzeros.data_ptr(), K, N, group,
+                                             out.data_ptr(), _stream(stream)), "w4a16_requant_pack")
     return out
 
 

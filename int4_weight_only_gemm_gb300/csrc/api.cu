@@ -159,6 +159,26 @@ int w4a16_unpack(const uint32_t* qweight_dev, uint32_t* qweight, int K, int N, w
     return W4A16_OK;
 }
 
+int w4a16_requant_pack(const void* w, const void* scales, const uint32_t* qzeros, int K, int N, int group,
+                       uint32_t* qweight_dev, w4a16_stream_t stream) {
+    if (!w || !scales || !qzeros || !qweight_dev) return W4A16_EINVAL;
+    if (group != 128) return W4A16_EUNSUPPORTED;
+    int st = check_kn(N, K);
+    if (st != W4A16_OK) return st;
+    if (K / 128 * 4 > 65535) return W4A16_EUNSUPPORTED;  // one grid row per 32-row chunk
+    if (!aligned16(w) || !aligned16(scales) || !aligned16(qzeros) || !aligned16(qweight_dev)) return W4A16_EALIGN;
+    const size_t qbytes = (size_t)K / 2 * N;
+    const int G = K / group;
+    if (overlaps(qweight_dev, qbytes, w, (size_t)K * N * 2) || overlaps(qweight_dev, qbytes, scales, (size_t)G * N * 2) ||
+        overlaps(qweight_dev, qbytes, qzeros, (size_t)G * N / 2))
+        return W4A16_EINVAL;
+    if (launch_requant_pack(static_cast<const uint16_t*>(w), static_cast<const uint16_t*>(scales), qzeros, qweight_dev,
+                            K, N, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return W4A16_ECUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return W4A16_OK;
+}
+
 size_t w4a16_workspace_bytes_path(int path, int M, int N, int K, int group) {
     if (M < 1 || group != 128 || check_kn(N, K) != W4A16_OK) return 0;
     const int dev = current_device();

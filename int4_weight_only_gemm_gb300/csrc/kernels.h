@@ -11,6 +11,8 @@ namespace w4a16 {
 
 cudaError_t launch_pack(const uint32_t* q, uint32_t* qd, int K, int N, cudaStream_t s);
 cudaError_t launch_unpack(const uint32_t* qd, uint32_t* q, int K, int N, cudaStream_t s);
+cudaError_t launch_requant_pack(const uint16_t* w, const uint16_t* scales, const uint32_t* qzeros, uint32_t* qd,
+                                int K, int N, cudaStream_t s);
 
 // CUDA-core split-K GEMV (M <= 8)
 struct GemvPlan {

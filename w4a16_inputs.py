@@ -120,3 +120,12 @@ def random_x(M: int, K: int, seed: int) -> np.ndarray:
     """Extra activation rows (bfloat16 bits) from an independent stream."""
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0xA11, M, K])))
     return f32_to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
+
+
+def random_weights(K: int, N: int, seed: int, sigma: float = 0.05) -> np.ndarray:
+    """Dense weights w[K][N] (bfloat16 bits) for the re-quantization step:
+    float32 normal draws with standard deviation `sigma`, rounded to bfloat16
+    (nearest, ties to even).  With scales in [0.001, 0.02], w / s spans well
+    past the 0..15 code range, so clipping is exercised too."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0x5EC, K, N])))
+    return f32_to_bf16_bits(rng.standard_normal((K, N), dtype=np.float32) * np.float32(sigma))
