@@ -9,54 +9,89 @@
 //
 // The pages give neither the rounding rule nor the precision: the decision is
 // taken in IEEE binary32 -- w and s are exact there, the quotient is the
-// correctly rounded one (__fdiv_rn), rounded to the nearest integer with ties
-// to even (rintf), then z is added and the sum clipped to 0..15.
+// correctly rounded one, rounded to the nearest integer with ties to even
+// (rintf), then z is added and the sum clipped to 0..15.
 //
-// One thread makes one column's 32 codes of one 32-row chunk: it reads 32
-// bf16 values (one per row; the threads of a block read each row's 128
-// columns as one contiguous run) and writes the chunk's four device words
-// with one 16-byte store (the block writes the chunk's 2 KB contiguously).
+// The quotient is needed only to the nearest integer, so it is first taken as
+// q0 = w * RN(1/s): with RN(1/s) = (1/s)(1 + e1) and one more rounding,
+// |q0 - w/s| <= (2^-24 + 2^-24 + 2^-48)|w/s|, and the correctly rounded
+// quotient Q is within 2^-24 |w/s| of w/s, so |q0 - Q| < 2^-21 max(|q0|, 1).
+// Unless a half-integer lies that close to q0, rint(q0) = rint(Q); in that
+// rare case (exact ties included) Q itself is computed with __fdiv_rn.
+//
+// One thread makes eight adjacent columns' codes of one 32-row chunk: per row
+// it reads the eight bf16 values with one 16-byte load (a warp reads 512
+// contiguous bytes), and it writes the eight columns' chunk words -- four
+// words each, adjacent in the device layout -- as 128 contiguous bytes.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace w4a16 {
+
+constexpr int kRqChunks = 8;  // 32-row chunks per block: 16 threads x 8 columns cover a tile row
 
 __global__ void __launch_bounds__(128) requant_pack_kernel(const uint16_t* __restrict__ w,
                                                            const uint16_t* __restrict__ scales,
                                                            const uint32_t* __restrict__ qzeros,
                                                            uint32_t* __restrict__ qd, int K, int N) {
     const Layout L(K, N);
-    const int nb = blockIdx.x;     // column tile
-    const int kb = blockIdx.y >> 2;  // 128-row group
-    const int c = blockIdx.y & 3;    // 32-row chunk of the group
+    const int nb = blockIdx.x;                                   // column tile
+    const int chunk = blockIdx.y * kRqChunks + (threadIdx.x >> 4);  // 32-row chunk of K
+    if (chunk >= 4 * L.KB) return;
+    const int kb = chunk >> 2, c = chunk & 3;
     const int W = L.width(nb);
-    const int t = threadIdx.x;
-    if (t >= W) return;
-    const int n = 128 * nb + t;
-    const float s = f16_bits_to_f32(scales[(size_t)kb * N + n]);
-    const float z = (float)((qzeros[(size_t)kb * (N / 8) + (n >> 3)] >> (4 * (n & 7))) & 0xFu);
-    const uint16_t* wp = w + (size_t)(128 * kb + 32 * c) * N + n;
-    uint32_t word[4];
+    const int t0 = (threadIdx.x & 15) * 8;                       // first of this thread's 8 columns
+    if (t0 >= W) return;                                         // W is a multiple of 8
+    const int n0 = 128 * nb + t0;
+    float s[8], rs[8], z[8];
+    {
+        const uint4 sv = *reinterpret_cast<const uint4*>(scales + (size_t)kb * N + n0);
+        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+        const uint32_t zw = qzeros[(size_t)kb * (N / 8) + (n0 >> 3)];  // n0 % 8 == 0: one word, 8 columns
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            s[e] = f16_bits_to_f32((uint16_t)(sw[e >> 1] >> (16 * (e & 1))));
+            rs[e] = __frcp_rn(s[e]);
+            z[e] = (float)((zw >> (4 * e)) & 0xFu);
+        }
+    }
+    const uint16_t* wp = w + (size_t)(128 * kb + 32 * c) * N + n0;
+    uint32_t word[8][4];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) word[e][j] = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        uint32_t o = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float wv = __uint_as_float((uint32_t)wp[(size_t)(8 * j + i) * N] << 16);  // bf16 -> binary32, exact
-            const float r = rintf(__fdiv_rn(wv, s));
-            const float v = fminf(fmaxf(r + z, 0.f), 15.f);
-            o |= (uint32_t)v << (4 * dev_nibble_pos(i));
+        for (int i = 0; i < 8; ++i) {  // row 8j + i of the chunk
+            const uint4 v = *reinterpret_cast<const uint4*>(wp + (size_t)(8 * j + i) * N);
+            const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+            const int sh = 4 * dev_nibble_pos(i);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float wv = __uint_as_float((e & 1) ? (vw[e >> 1] & 0xFFFF0000u) : (vw[e >> 1] << 16));  // exact
+                const float q0 = __fmul_rn(wv, rs[e]);
+                float r = rintf(q0);
+                // distance from q0 to the nearest half-integer against the bound;
+                // a non-finite q0 fails the test and takes the exact path too
+                if (!(fabsf(0.5f - fabsf(q0 - r)) > 0x1p-20f * fmaxf(fabsf(q0), 1.f)))
+                    r = rintf(__fdiv_rn(wv, s[e]));
+                const float q = fminf(fmaxf(r + z[e], 0.f), 15.f);
+                word[e][j] |= (uint32_t)q << sh;
+            }
         }
-        word[j] = o;
     }
-    *reinterpret_cast<uint4*>(qd + L.block_word(nb, kb) + ((size_t)c * W + t) * 4) =
-        make_uint4(word[0], word[1], word[2], word[3]);
+    uint4* dst = reinterpret_cast<uint4*>(qd + L.block_word(nb, kb) + ((size_t)c * W + t0) * 4);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dst[e] = make_uint4(word[e][0], word[e][1], word[e][2], word[e][3]);
 }
 
 cudaError_t launch_requant_pack(const uint16_t* w, const uint16_t* scales, const uint32_t* qzeros, uint32_t* qd,
                                 int K, int N, cudaStream_t s) {
     const Layout L(K, N);
-    requant_pack_kernel<<<dim3(L.NB, 4 * L.KB), 128, 0, s>>>(w, scales, qzeros, qd, K, N);
+    requant_pack_kernel<<<dim3(L.NB, (4 * L.KB + kRqChunks - 1) / kRqChunks), 128, 0, s>>>(w, scales, qzeros, qd, K,
+                                                                                         N);
     return cudaGetLastError();
 }
 
