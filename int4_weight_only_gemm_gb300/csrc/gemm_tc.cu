@@ -12,20 +12,26 @@
 // roles walk the same sequence of (unit, group) pairs, numbered q = 0, 1, ...
 // One pipeline stage carries one group of 128 rows of K.
 //
-//  * producer warp: per group, into ring stage q % SS: the packed weight slab
-//    (bulk copy, 8 KB for a full tile), the group's scales (bulk copy), its
-//    zero-point words (4-byte cp.async) and the x tile (two TMA boxes of
-//    NT x 64 bf16, 128-byte swizzle), all completing one barrier;
-//  * two dequant warpgroups, taking alternate groups: thread t turns column
-//    t's 16 words into 64 bfloat16 pairs (q - z) -- exact small integers:
-//    mask-and-or to 128 + q, subtract 128 + z -- and writes them to tensor
-//    memory as the MMA's A operand (tcgen05.st, buffer q % 4); after a
-//    warpgroup barrier one of its threads issues the group's 8 tcgen05.mma
-//    kind::f16 (A from TMEM, B = x from shared memory) into D buffer q % 2;
+//  * weight producer warp: per group, into ring stage q % SS, the packed
+//    weight slab (one bulk copy, 8 KB for a full tile) and the group's
+//    zero-point words; activation producer warp: the x tile (one 3-D TMA,
+//    two 64-wide 128-byte swizzled slabs); both complete one barrier;
+//  * dequant warpgroups (four for NT <= 32, two for NT = 128), taking groups
+//    in turn: thread t turns column t's 16 words into 64 bfloat16 pairs
+//    (q - z) -- exact small integers: mask-and-or to 128 + q, subtract
+//    128 + z -- and writes them to tensor memory as the MMA's A operand
+//    (tcgen05.st, buffer q % SA);
+//  * MMA warp: one elected lane issues each group's 8 tcgen05.mma kind::f16
+//    (A from tensor memory, B = x from shared memory) into D buffer q % NDB
+//    and commits them to the group's barrier;
 //  * rescale warpgroup(s): per group, reads D with tcgen05.ld and adds
 //    s[g][n] * D into f32 registers (the binary16 scale is applied in f32,
 //    never rounded to bfloat16); at a unit's end writes bf16 y, or split-K
 //    partials reduced in fixed order by the last CTA to arrive.
+//
+// For NT = 128 a rescale thread holds 64 accumulators: its warpgroups raise
+// their register budget (setmaxnreg) with registers the dequant warpgroups and
+// the MMA / producer warpgroup give back, so nothing spills.
 //
 // Every wait is bounded (common.cuh).  After a timeout every role keeps
 // walking its loop without doing work, so all barriers still meet; the CTA
@@ -60,7 +66,7 @@ template <int NT>
 struct TcCfg {
     static constexpr int R = NT >= 128 ? 2 : 1;          // rescale warpgroups, each owning NT/R columns
     static constexpr int SS = NT <= 16 ? 12 : NT <= 32 ? 10 : 4;  // shared-memory ring stages
-    static constexpr int SA = NT <= 32 ? 4 : 2;          // A buffers in tensor memory (q % SA)
+    static constexpr int SA = NT <= 32 ? 4 : 3;          // A buffers in tensor memory (q % SA)
     static constexpr int NDB = ((512 - SA * 64) / NT) < 8 ? ((512 - SA * 64) / NT) : 8;  // D accumulator ring
     static constexpr int kDone = 16;                     // ring of "MMAs of group q done" barriers
     static constexpr int kDeqWG = NT <= 32 ? 4 : 2;      // dequant warpgroups, taking groups q % kDeqWG
@@ -69,7 +75,18 @@ struct TcCfg {
     static constexpr int kMmaWarp = kDeqWarps + 4 * R;   // then the MMA warp (the only tcgen05.mma issuer)
     static constexpr int kProdWarp = kMmaWarp + 1;       // weight producer (also owns TMEM)
     static constexpr int kXWarp = kProdWarp + 1;         // activation producer
-    static constexpr int kThreads = 32 * (kXWarp + 1);
+    // NT = 128: a rescale thread holds 64 f32 accumulators, more than an even
+    // share of the register file allows, so the rescale warpgroups take
+    // registers from the other roles (setmaxnreg).  Every role is then whole
+    // warpgroups: the last one, MMA + producers, is padded with an idle warp.
+    static constexpr bool kRegSplit = NT >= 128;
+    static constexpr int kWarps = kRegSplit ? (kXWarp + 4) / 4 * 4 : kXWarp + 1;
+    static constexpr int kThreads = 32 * kWarps;
+    static constexpr int kRegDeq = 72, kRegRes = 136, kRegMisc = 64;  // per thread, after the split
+    static constexpr int kRegPool =
+        32 * (kDeqWarps * kRegDeq + 4 * R * kRegRes + (kWarps - kDeqWarps - 4 * R) * kRegMisc);
+    static_assert(!kRegSplit || kRegPool <= kThreads * 96, "register split above a 96-register launch");
+    static_assert(!kRegSplit || (kDeqWarps % 4 == 0 && kMmaWarp % 4 == 0), "roles must be whole warpgroups");
     static_assert(SS <= kDone && SA <= kDone && NDB <= kDone, "barrier ring too short for the phase parity");
     // shared memory, from a 1024-byte aligned base
     static constexpr int kXStage = NT * 256;             // two swizzled boxes of NT rows x 128 bytes
@@ -182,76 +199,122 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
     const uint32_t tmem = *tmem_holder;
     if (warp != C::kProdWarp && warp != C::kXWarp) pdl_wait();  // producers wait in their own loops
 
-    if (warp == C::kProdWarp) {
-        // ------------------------------------------------ weight producer
-        // Per group, into ring stage q % SS: the packed weight slab and the
-        // zero-point words.  The zero words are 16-byte aligned when
-        // N % 32 == 0 and then come in one bulk copy; otherwise lane 0 fetches
-        // them with 4-byte async copies.
-        int q = 0, issued = 0;
-        bool ok = true;
-        const bool zbulk = p.N % 32 == 0;
-        // This warp touches only weights and zeros: with static weights it
-        // never waits on the preceding grid, otherwise once before any load.
-        if (!p.prefetch) pdl_wait();
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-            const UnitInfo ui = unit_info(p, u);
-            const int W = L.width(ui.nb);
-            const uint32_t wbytes = (uint32_t)W * 64;
-            const uint32_t zbytes = zbulk ? (uint32_t)(W / 2) : 0u;
-            const uint32_t* wsrc = p.qd + L.block_word(ui.nb, ui.g0);
-            const uint32_t* zsrc = p.qzeros + (size_t)ui.g0 * (p.N / 8) + 16 * ui.nb;
-            for (int g = ui.g0; g < ui.g1; ++g, ++q, wsrc += W * 16, zsrc += p.N / 8) {
-                const int s = q % SS;
-                // stage s is free once the MMAs of group q - SS are done
-                if (ok && q >= SS &&
-                    !mbar_wait_warp(&done[(q - SS) % ND], ((q - SS) / ND) & 1, abort_flag, &g_tc_status))
-                    ok = false;
-                if (ok) {
-                    if (lane == 0) {
-                        if (!zbulk) {
-                            for (int i = 0; i < W / 8; ++i) cp_async_4(smem + C::kZOff + s * 64 + i * 4, zsrc + i);
-                            cp_async_mbar_arrive(&full[s]);
+    if (warp >= C::kMmaWarp) {
+        // MMA issue, weight and activation producers, and (with the
+        // register split) an idle warp: one warpgroup
+        if constexpr (C::kRegSplit) regs_dec<C::kRegMisc>();
+        if (warp == C::kProdWarp) {
+            // ------------------------------------------------ weight producer
+            // Per group, into ring stage q % SS: the packed weight slab and the
+            // zero-point words.  The zero words are 16-byte aligned when
+            // N % 32 == 0 and then come in one bulk copy; otherwise lane 0 fetches
+            // them with 4-byte async copies.
+            int q = 0, issued = 0;
+            bool ok = true;
+            const bool zbulk = p.N % 32 == 0;
+            // This warp touches only weights and zeros: with static weights it
+            // never waits on the preceding grid, otherwise once before any load.
+            if (!p.prefetch) pdl_wait();
+            for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+                const UnitInfo ui = unit_info(p, u);
+                const int W = L.width(ui.nb);
+                const uint32_t wbytes = (uint32_t)W * 64;
+                const uint32_t zbytes = zbulk ? (uint32_t)(W / 2) : 0u;
+                const uint32_t* wsrc = p.qd + L.block_word(ui.nb, ui.g0);
+                const uint32_t* zsrc = p.qzeros + (size_t)ui.g0 * (p.N / 8) + 16 * ui.nb;
+                for (int g = ui.g0; g < ui.g1; ++g, ++q, wsrc += W * 16, zsrc += p.N / 8) {
+                    const int s = q % SS;
+                    // stage s is free once the MMAs of group q - SS are done
+                    if (ok && q >= SS &&
+                        !mbar_wait_warp(&done[(q - SS) % ND], ((q - SS) / ND) & 1, abort_flag, &g_tc_status))
+                        ok = false;
+                    if (ok) {
+                        if (lane == 0) {
+                            if (!zbulk) {
+                                for (int i = 0; i < W / 8; ++i) cp_async_4(smem + C::kZOff + s * 64 + i * 4, zsrc + i);
+                                cp_async_mbar_arrive(&full[s]);
+                            }
+                            mbar_arrive_expect_tx(&full[s], wbytes + zbytes);
+                            bulk_g2s(smem + C::kPOff + s * 8192, wsrc, wbytes, &full[s]);
+                            if (zbulk) bulk_g2s(smem + C::kZOff + s * 64, zsrc, zbytes, &full[s]);
                         }
-                        mbar_arrive_expect_tx(&full[s], wbytes + zbytes);
-                        bulk_g2s(smem + C::kPOff + s * 8192, wsrc, wbytes, &full[s]);
-                        if (zbulk) bulk_g2s(smem + C::kZOff + s * 64, zsrc, zbytes, &full[s]);
+                        __syncwarp();
+                        issued = q + 1;
                     }
-                    __syncwarp();
-                    issued = q + 1;
                 }
             }
-        }
-        // drain: every stage armed must land before the CTA may exit
-        for (int i = issued > SS ? issued - SS : 0; i < issued; ++i)
-            (void)mbar_wait(&full[i % SS], (i / SS) & 1, nullptr, &g_tc_status);
-    } else if (warp == C::kXWarp) {
-        // -------------------------------------------- activation producer
-        // Per group: x[tile tokens][128 rows of K] with one 3-D TMA (two
-        // 64-wide, 128-byte swizzled slabs).  Always after the preceding grid.
-        pdl_wait();
-        int q = 0, issued = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-            const UnitInfo ui = unit_info(p, u);
-            for (int g = ui.g0; g < ui.g1; ++g, ++q) {
-                const int s = q % SS;
-                if (ok && q >= SS &&
-                    !mbar_wait_warp(&done[(q - SS) % ND], ((q - SS) / ND) & 1, abort_flag, &g_tc_status))
-                    ok = false;
-                if (ok) {
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(&full[s], (uint32_t)C::kXStage);
-                        tma_load_3d(smem + C::kXOff + s * C::kXStage, &tmap_x, 0, ui.mb * NT, 2 * g, &full[s]);
+            // drain: every stage armed must land before the CTA may exit
+            for (int i = issued > SS ? issued - SS : 0; i < issued; ++i)
+                (void)mbar_wait(&full[i % SS], (i / SS) & 1, nullptr, &g_tc_status);
+        } else if (warp == C::kXWarp) {
+            // -------------------------------------------- activation producer
+            // Per group: x[tile tokens][128 rows of K] with one 3-D TMA (two
+            // 64-wide, 128-byte swizzled slabs).  Always after the preceding grid.
+            pdl_wait();
+            int q = 0, issued = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+                const UnitInfo ui = unit_info(p, u);
+                for (int g = ui.g0; g < ui.g1; ++g, ++q) {
+                    const int s = q % SS;
+                    if (ok && q >= SS &&
+                        !mbar_wait_warp(&done[(q - SS) % ND], ((q - SS) / ND) & 1, abort_flag, &g_tc_status))
+                        ok = false;
+                    if (ok) {
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(&full[s], (uint32_t)C::kXStage);
+                            tma_load_3d(smem + C::kXOff + s * C::kXStage, &tmap_x, 0, ui.mb * NT, 2 * g, &full[s]);
+                        }
+                        __syncwarp();
+                        issued = q + 1;
                     }
-                    __syncwarp();
-                    issued = q + 1;
                 }
             }
+            for (int i = issued > SS ? issued - SS : 0; i < issued; ++i)
+                (void)mbar_wait(&full[i % SS], (i / SS) & 1, nullptr, &g_tc_status);
+        } else if (warp == C::kMmaWarp) {
+            // ------------------------------------------------------------ MMA issue
+            // The one thread of the CTA that issues tcgen05.mma: the whole loop runs
+            // in an elected lane, so a barrier that has already completed costs a
+            // single poll and no warp vote.  It needs only the flat group index q.
+            constexpr uint32_t idesc = idesc_bf16_f32(128, NT);
+            int Q = 0;  // groups this CTA processes
+            for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+                const UnitInfo ui = unit_info(p, u);
+                Q += ui.g1 - ui.g0;
+            }
+            if (elect_one()) {
+                bool ok = true;
+                for (int q = 0; q < Q; ++q) {
+                    if (!mbar_wait(&a_full[q % SA], (q / SA) & 1, abort_flag, &g_tc_status)) ok = false;
+                    // D buffer q % NDB is free once every rescale warp has read group q - NDB
+                    if (ok && q >= C::NDB &&
+                        !mbar_wait(&d_empty[q % C::NDB], ((q / C::NDB) - 1) & 1, abort_flag, &g_tc_status))
+                        ok = false;
+                    if (!ok) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xaddr = smem_u32(smem + C::kXOff + (q % SS) * C::kXStage);
+                    const uint32_t a_tmem = tmem + C::kTmemA + (q % SA) * 64;
+                    const uint32_t d_tmem = tmem + C::kTmemD + (q % C::NDB) * NT;
+    #pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t bdesc = smem_desc_sw128(xaddr + (kk >> 2) * (NT * 128) + (kk & 3) * 32);
+                        mma_bf16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&done[q % ND]);
+                }
+                // every MMA issued must be complete before TMEM is freed
+                mma_commit(mma_done);
+            }
+            __syncwarp();
+            pdl_launch_dependents();  // this CTA issues no more tensor work
+            (void)mbar_wait(mma_done, 0, nullptr, &g_tc_status);
         }
-        for (int i = issued > SS ? issued - SS : 0; i < issued; ++i)
-            (void)mbar_wait(&full[i % SS], (i / SS) & 1, nullptr, &g_tc_status);
     } else if (warp < C::kDeqWarps) {
+        if constexpr (C::kRegSplit) regs_dec<C::kRegDeq>();
         // ------------------------------------------------------------ dequant
         const int h = warp >> 2;              // warpgroup: takes groups q with q % kDeqWG == h
         const int quad = warp & 3;            // TMEM lane quadrant
@@ -310,54 +373,15 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                 if (!ok) *abort_flag = 1;
             }
         }
-    } else if (warp == C::kMmaWarp) {
-        // ------------------------------------------------------------ MMA issue
-        // The one thread of the CTA that issues tcgen05.mma: the whole loop runs
-        // in an elected lane, so a barrier that has already completed costs a
-        // single poll and no warp vote.  It needs only the flat group index q.
-        constexpr uint32_t idesc = idesc_bf16_f32(128, NT);
-        int Q = 0;  // groups this CTA processes
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-            const UnitInfo ui = unit_info(p, u);
-            Q += ui.g1 - ui.g0;
-        }
-        if (elect_one()) {
-            bool ok = true;
-            for (int q = 0; q < Q; ++q) {
-                if (!mbar_wait(&a_full[q % SA], (q / SA) & 1, abort_flag, &g_tc_status)) ok = false;
-                // D buffer q % NDB is free once every rescale warp has read group q - NDB
-                if (ok && q >= C::NDB &&
-                    !mbar_wait(&d_empty[q % C::NDB], ((q / C::NDB) - 1) & 1, abort_flag, &g_tc_status))
-                    ok = false;
-                if (!ok) {
-                    *abort_flag = 1;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t xaddr = smem_u32(smem + C::kXOff + (q % SS) * C::kXStage);
-                const uint32_t a_tmem = tmem + C::kTmemA + (q % SA) * 64;
-                const uint32_t d_tmem = tmem + C::kTmemD + (q % C::NDB) * NT;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bdesc = smem_desc_sw128(xaddr + (kk >> 2) * (NT * 128) + (kk & 3) * 32);
-                    mma_bf16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&done[q % ND]);
-            }
-            // every MMA issued must be complete before TMEM is freed
-            mma_commit(mma_done);
-        }
-        __syncwarp();
-        pdl_launch_dependents();  // this CTA issues no more tensor work
-        (void)mbar_wait(mma_done, 0, nullptr, &g_tc_status);
     } else {
+        if constexpr (C::kRegSplit) regs_inc<C::kRegRes>();
         // ------------------------------------------------------- rescale + epilogue
         const int r = (warp - C::kResWarp0) >> 2;  // rescale warpgroup: owns columns [r*CW, (r+1)*CW)
         const int quad = warp & 3;
         const int t = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         constexpr int CW = NT / R;                 // columns (tokens) per rescale warpgroup
-        constexpr int kBatch = CW < 32 ? CW : (CW >= 64 ? 16 : 32);  // columns read from TMEM per wait
+        constexpr int kBatch = CW < 32 ? CW : (CW >= 64 && !C::kRegSplit ? 16 : 32);  // columns read from TMEM per wait
         const int rt = r * 128 + t;                // thread index among the rescale warpgroups
         float2 acc[CW / 2];
 #pragma unroll
@@ -595,6 +619,14 @@ static cudaError_t launch_nt(const CUtensorMap& tm, const TcParams& prm, const T
     if (!set_for[dev]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<NT>::kAlloc);
         if (e != cudaSuccess) return e;
+        if (TcCfg<NT>::kRegSplit) {
+            // the warpgroups' register budgets must fit in what the CTA is
+            // launched with, or the increase would wait forever: never launch then
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, kern);
+            if (e != cudaSuccess) return e;
+            if ((long long)fa.numRegs * TcCfg<NT>::kThreads < TcCfg<NT>::kRegPool) return cudaErrorInvalidConfiguration;
+        }
         set_for[dev] = 1;
     }
     return launch_kernel(kern, dim3(plan.ctas), dim3(TcCfg<NT>::kThreads), plan.smem, s, pdl, tm, prm);
