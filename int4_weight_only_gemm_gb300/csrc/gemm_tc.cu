@@ -82,7 +82,7 @@ struct TcCfg {
     static constexpr bool kRegSplit = NT >= 128;
     static constexpr int kWarps = kRegSplit ? (kXWarp + 4) / 4 * 4 : kXWarp + 1;
     static constexpr int kThreads = 32 * kWarps;
-    static constexpr int kRegDeq = 72, kRegRes = 136, kRegMisc = 64;  // per thread, after the split
+    static constexpr int kRegDeq = 64, kRegRes = 144, kRegMisc = 64;  // per thread, after the split
     static constexpr int kRegPool =
         32 * (kDeqWarps * kRegDeq + 4 * R * kRegRes + (kWarps - kDeqWarps - 4 * R) * kRegMisc);
     static_assert(!kRegSplit || kRegPool <= kThreads * 96, "register split above a 96-register launch");
@@ -381,7 +381,8 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
         const int t = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         constexpr int CW = NT / R;                 // columns (tokens) per rescale warpgroup
-        constexpr int kBatch = CW < 32 ? CW : (CW >= 64 && !C::kRegSplit ? 16 : 32);  // columns read from TMEM per wait
+        // columns read from tensor memory per wait: all of them where registers allow
+        constexpr int kBatch = CW <= 32 || C::kRegSplit ? CW : 16;
         const int rt = r * 128 + t;                // thread index among the rescale warpgroups
         float2 acc[CW / 2];
 #pragma unroll
@@ -429,21 +430,38 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                     tc_fence_after();
                     const float2 sc2 = make_float2(sc, sc);
                     const uint32_t dbase = tmem + lane_base + C::kTmemD + b * NT + r * CW;
+                    if constexpr (C::kRegSplit) {
+                        // all columns in one load: the D buffer goes back to the
+                        // MMA before the multiply-adds
+                        uint32_t v[CW];
 #pragma unroll
-                    for (int c0 = 0; c0 < CW; c0 += kBatch) {
-                        uint32_t v[kBatch];
-#pragma unroll
-                        for (int c = 0; c < kBatch; c += 16)
-                            tmem_ld_x16(dbase + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(v + c));
+                        for (int c = 0; c < CW; c += 16)
+                            tmem_ld_x16(dbase + c, *reinterpret_cast<uint32_t(*)[16]>(v + c));
                         tmem_wait_ld();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&d_empty[b]);
 #pragma unroll
-                        for (int i = 0; i < kBatch; i += 2)
-                            acc[(c0 + i) / 2] = __ffma2_rn(
-                                sc2, make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), acc[(c0 + i) / 2]);
+                        for (int i = 0; i < CW; i += 2)
+                            acc[i / 2] = __ffma2_rn(sc2, make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                                    acc[i / 2]);
+                    } else {
+#pragma unroll
+                        for (int c0 = 0; c0 < CW; c0 += kBatch) {
+                            uint32_t v[kBatch];
+#pragma unroll
+                            for (int c = 0; c < kBatch; c += 16)
+                                tmem_ld_x16(dbase + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(v + c));
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < kBatch; i += 2)
+                                acc[(c0 + i) / 2] = __ffma2_rn(
+                                    sc2, make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), acc[(c0 + i) / 2]);
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&d_empty[b]);
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&d_empty[b]);
                 }
                 // the slot just read is refilled only after sc was consumed above
                 issue_scale(q % C::kSP);
