@@ -251,19 +251,6 @@ W4A16_DEVICE void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 W4A16_DEVICE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 W4A16_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Per-thread register budget of the calling warpgroup (all four warps execute
-// the same one).  A decrease returns registers to the CTA's pool, an increase
-// waits until the pool holds them: the budgets of all warpgroups together must
-// not exceed the registers the CTA was launched with.
-template <int N>
-W4A16_DEVICE void regs_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-W4A16_DEVICE void regs_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // D[tmem] (+)= A[tmem] * B[smem desc], kind::f16 (bf16 inputs, f32 accumulate)
 W4A16_DEVICE void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                               uint32_t accumulate) {

@@ -45,6 +45,18 @@
 namespace w4a16 {
 
 static __device__ int g_tc_status;
+// Per-thread register budget of the calling warpgroup (all four warps execute
+// the same one).  A decrease returns registers to the CTA's pool, an increase
+// waits until the pool holds them: the budgets of all warpgroups together must
+// not exceed the registers the CTA was launched with.
+template <int N>
+W4A16_DEVICE void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+W4A16_DEVICE void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 struct TcParams {
     const uint32_t* qd;
