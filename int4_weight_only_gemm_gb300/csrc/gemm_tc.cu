@@ -16,7 +16,7 @@
 //    weight slab (one bulk copy, 8 KB for a full tile) and the group's
 //    zero-point words; activation producer warp: the x tile (one 3-D TMA,
 //    two 64-wide 128-byte swizzled slabs); both complete one barrier;
-//  * dequant warpgroups (four for NT <= 32, two for NT = 128), taking groups
+//  * dequant warpgroups (four for NT <= 32, two for NT = 128 / 192), taking groups
 //    in turn: thread t turns column t's 16 words into 64 bfloat16 pairs
 //    (q - z) -- exact small integers: mask-and-or to 128 + q, subtract
 //    128 + z -- and writes them to tensor memory as the MMA's A operand
@@ -29,7 +29,7 @@
 //    never rounded to bfloat16); at a unit's end writes bf16 y, or split-K
 //    partials reduced in fixed order by the last CTA to arrive.
 //
-// For NT = 128 a rescale thread holds 64 accumulators: its warpgroups raise
+// For NT >= 128 a rescale thread holds 64 or 96 accumulators: its warpgroups raise
 // their register budget (setmaxnreg) with registers the dequant warpgroups and
 // the MMA / producer warpgroup give back, so nothing spills.
 //
@@ -77,17 +77,21 @@ struct TcParams {
 template <int NT>
 struct TcCfg {
     static constexpr int R = NT >= 128 ? 2 : 1;          // rescale warpgroups, each owning NT/R columns
-    static constexpr int SS = NT <= 16 ? 12 : NT <= 32 ? 10 : 4;  // shared-memory ring stages
-    static constexpr int SA = NT <= 32 ? 4 : 3;          // A buffers in tensor memory (q % SA)
+    static constexpr int SS = NT <= 16 ? 12 : NT <= 32 ? 10 : NT <= 128 ? 4 : 3;  // shared-memory ring stages
+    static constexpr int SA = NT <= 32 ? 4 : NT <= 128 ? 3 : 2;  // A buffers in tensor memory (q % SA)
     static constexpr int NDB = ((512 - SA * 64) / NT) < 8 ? ((512 - SA * 64) / NT) : 8;  // D accumulator ring
     static constexpr int kDone = 16;                     // ring of "MMAs of group q done" barriers
+    // ring of "group q may be issued" barriers: its A buffer written and its D
+    // buffer read out (arrivals for q follow the completion of q - SA and of
+    // q - NDB, so max(SA, NDB) slots keep the phases apart)
+    static constexpr int kReady = SA > NDB ? SA : NDB;
     static constexpr int kDeqWG = NT <= 32 ? 4 : 2;      // dequant warpgroups, taking groups q % kDeqWG
     static constexpr int kDeqWarps = 4 * kDeqWG;
     static constexpr int kResWarp0 = kDeqWarps;          // rescale warpgroups follow
     static constexpr int kMmaWarp = kDeqWarps + 4 * R;   // then the MMA warp (the only tcgen05.mma issuer)
     static constexpr int kProdWarp = kMmaWarp + 1;       // weight producer (also owns TMEM)
     static constexpr int kXWarp = kProdWarp + 1;         // activation producer
-    // NT = 128: a rescale thread holds 64 f32 accumulators, more than an even
+    // NT >= 128: a rescale thread holds 64 or 96 f32 accumulators, more than an even
     // share of the register file allows, so the rescale warpgroups take
     // registers from the other roles (setmaxnreg).  Every role is then whole
     // warpgroups: the last one, MMA + producers, is padded with an idle warp.
@@ -100,6 +104,7 @@ struct TcCfg {
     static_assert(!kRegSplit || kRegPool <= kThreads * 96, "register split above a 96-register launch");
     static_assert(!kRegSplit || (kDeqWarps % 4 == 0 && kMmaWarp % 4 == 0), "roles must be whole warpgroups");
     static_assert(SS <= kDone && SA <= kDone && NDB <= kDone, "barrier ring too short for the phase parity");
+    static_assert(SS + kDone + kReady + 1 <= 128, "barriers are initialised by the first threads");
     // shared memory, from a 1024-byte aligned base
     static constexpr int kXStage = NT * 256;             // two swizzled boxes of NT rows x 128 bytes
     static constexpr int kXOff = 0;
@@ -176,9 +181,10 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* full = bars;                 // [SS] stage landed (transactions + cp.async)
     uint64_t* done = bars + SS;            // [ND] all MMAs of group q finished: done[q % ND]
-    uint64_t* a_full = done + ND;          // [SA] A buffer q % SA written (4 dequant warps)
-    uint64_t* d_empty = a_full + SA;       // [NDB] D buffer read by every rescale warp
-    uint64_t* mma_done = d_empty + C::NDB; // [1] every MMA of the CTA finished
+    // [kReady] group q may be issued: A buffer q % SA written (4 dequant warps)
+    // and D buffer q % NDB read out for group q - NDB (every rescale warp)
+    uint64_t* ready = done + ND;
+    uint64_t* mma_done = ready + C::kReady;  // [1] every MMA of the CTA finished
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     int* sh_last = const_cast<int*>(abort_flag) + 1;
@@ -192,13 +198,12 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
         const int i = threadIdx.x;
         if (i < SS) mbar_init(&full[i], 2);  // one arrival per producer warp
         else if (i < SS + ND) mbar_init(&done[i - SS], 1);
-        else if (i < SS + ND + SA) mbar_init(&a_full[i - SS - ND], 4);
-        else if (i < SS + ND + SA + C::NDB) mbar_init(&d_empty[i - SS - ND - SA], 4 * R);
-        else if (i == SS + ND + SA + C::NDB) {
+        else if (i < SS + ND + C::kReady) mbar_init(&ready[i - SS - ND], 4 + 4 * R);
+        else if (i == SS + ND + C::kReady) {
             mbar_init(mma_done, 1);
             *abort_flag = 0;
         }
-        if (i <= SS + ND + SA + C::NDB) fence_mbar_init();
+        if (i <= SS + ND + C::kReady) fence_mbar_init();
     }
     if (warp == C::kProdWarp) {
         tmem_alloc(tmem_holder, C::kTmemCols);
@@ -298,11 +303,8 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
             if (elect_one()) {
                 bool ok = true;
                 for (int q = 0; q < Q; ++q) {
-                    if (!mbar_wait(&a_full[q % SA], (q / SA) & 1, abort_flag, &g_tc_status)) ok = false;
-                    // D buffer q % NDB is free once every rescale warp has read group q - NDB
-                    if (ok && q >= C::NDB &&
-                        !mbar_wait(&d_empty[q % C::NDB], ((q / C::NDB) - 1) & 1, abort_flag, &g_tc_status))
-                        ok = false;
+                    // A buffer q % SA written and D buffer q % NDB free: one poll
+                    if (!mbar_wait(&ready[q % C::kReady], (q / C::kReady) & 1, abort_flag, &g_tc_status)) ok = false;
                     if (!ok) {
                         *abort_flag = 1;
                         break;
@@ -380,7 +382,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&a_full[q % SA]);
+                    if (lane == 0) mbar_arrive(&ready[q % C::kReady]);
                 }
                 if (!ok) *abort_flag = 1;
             }
@@ -394,7 +396,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         constexpr int CW = NT / R;                 // columns (tokens) per rescale warpgroup
         // columns read from tensor memory per wait: all of them where registers allow
-        constexpr int kBatch = CW <= 32 || C::kRegSplit ? CW : 16;
+        constexpr int kBatch = CW <= 32 || (C::kRegSplit && CW <= 64) ? CW : C::kRegSplit ? 32 : 16;
         const int rt = r * 128 + t;                // thread index among the rescale warpgroups
         float2 acc[CW / 2];
 #pragma unroll
@@ -426,6 +428,9 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
         };
 #pragma unroll 1
         for (int i = 0; i < C::kSP; ++i) issue_scale(i);
+        // the D buffers of the first NDB groups start out free
+        if (lane == 0)
+            for (int i = 0; i < C::NDB; ++i) mbar_arrive(&ready[i]);
         int q = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
@@ -442,7 +447,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                     tc_fence_after();
                     const float2 sc2 = make_float2(sc, sc);
                     const uint32_t dbase = tmem + lane_base + C::kTmemD + b * NT + r * CW;
-                    if constexpr (C::kRegSplit) {
+                    if constexpr (C::kRegSplit && kBatch == CW) {
                         // all columns in one load: the D buffer goes back to the
                         // MMA before the multiply-adds
                         uint32_t v[CW];
@@ -452,7 +457,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                         tmem_wait_ld();
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&d_empty[b]);
+                        if (lane == 0) mbar_arrive(&ready[(q + C::NDB) % C::kReady]);  // D buffer b free for group q + NDB
 #pragma unroll
                         for (int i = 0; i < CW; i += 2)
                             acc[i / 2] = __ffma2_rn(sc2, make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
@@ -472,7 +477,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                         }
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&d_empty[b]);
+                        if (lane == 0) mbar_arrive(&ready[(q + C::NDB) % C::kReady]);  // D buffer b free for group q + NDB
                     }
                 }
                 // the slot just read is refilled only after sc was consumed above
@@ -565,7 +570,12 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-static int tc_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 128; }
+// Token tile.  An MMA of N <= 128 takes about as long as one of N = 128
+// (~47 ns for M = 128, K = 16, measured), while N = 256 runs at the full rate,
+// so large M takes 192-token tiles: two D buffers of 192 columns still fit
+// beside two A buffers in the 512 tensor-memory columns.  Up to 256 tokens
+// the shorter per-group chain of 128-token tiles measured faster.
+static int tc_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 256 ? 128 : 192; }
 
 bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
     const Layout L(K, N);
@@ -614,7 +624,10 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
     out->splits = splits;
     out->units = (int)units;
     out->ctas = (int)(units < slots ? units : slots);
-    out->smem = NT == 16 ? TcCfg<16>::kAlloc : NT == 32 ? TcCfg<32>::kAlloc : TcCfg<128>::kAlloc;
+    out->smem = NT == 16    ? TcCfg<16>::kAlloc
+                : NT == 32  ? TcCfg<32>::kAlloc
+                : NT == 128 ? TcCfg<128>::kAlloc
+                            : TcCfg<192>::kAlloc;
     const long long split_tiles = tiles - whole;
     out->ws_bytes = split_tiles > 0
                         ? ws_counter_bytes((size_t)split_tiles) + (size_t)split_tiles * splits * NT * 128 * sizeof(float)
@@ -700,6 +713,7 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
     switch (plan.NT) {
         case 16: return launch_nt<16>(tm, prm, plan, s, pdl);
         case 32: return launch_nt<32>(tm, prm, plan, s, pdl);
+        case 192: return launch_nt<192>(tm, prm, plan, s, pdl);
         default: return launch_nt<128>(tm, prm, plan, s, pdl);
     }
 }

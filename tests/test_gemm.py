@@ -116,7 +116,7 @@ def test_vocab_shape(M, path):
 # ---- edge cases: ragged tiles, odd M, one group --------------------------------
 
 EDGE = [(M, K, N) for (K, N) in [(128, 8), (128, 136), (384, 264), (1024, 392)]
-        for M in (1, 3, 7, 13, 17, 31, 33, 100, 129)]
+        for M in (1, 3, 7, 13, 17, 31, 33, 100, 129, 257, 400)]
 
 
 @pytest.mark.parametrize("M,K,N", EDGE)
@@ -129,7 +129,7 @@ def test_ragged_and_odd_shapes(M, K, N):
         check_close(bf16_to_f64(d.run(path)), ref, f"M={M} K={K} N={N} path={path}")
 
 
-@pytest.mark.parametrize("M", [1, 5, 16, 40])
+@pytest.mark.parametrize("M", [1, 5, 16, 40, 300])
 def test_exact_case_bit_exact(M):
     """x in {-1, 0, 1} with at most 8 nonzeros per row and s = 2^-6: every
     partial sum is exact in f32 and y*64 is an integer of magnitude <= 120, so
