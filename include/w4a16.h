@@ -186,6 +186,44 @@ int w4a16_gemm_ex(int path, unsigned flags, const void *x, const uint32_t *qweig
                   const void *scales, const uint32_t *qzeros, int M, int N, int K, int group,
                   void *y, void *workspace, size_t workspace_bytes, w4a16_stream_t stream);
 
+/*
+ * Fused gate/up projection of a gated MLP with its SiLU-multiply epilogue:
+ *
+ *     y[m][h] = silu(g[m][h]) * u[m][h],   silu(g) = g / (1 + exp(-g)),
+ *     g = x . dequant(W[:, h]),  u = x . dequant(W[:, H + h]),  0 <= h < H,
+ *
+ * for one weight matrix W of [K][2H] whose columns 0..H-1 are the gate
+ * projection and H..2H-1 the up projection, quantized with one grid (scales
+ * [K/group][2H], zeros [K/group][2H/8], canonical layout as for w4a16_gemm).
+ * g and u are accumulated in f32 exactly as w4a16_gemm accumulates y; the
+ * epilogue is evaluated in f32 and rounded once to bf16, so the [M][2H]
+ * intermediate is never written.
+ *
+ * The packed weights come from w4a16_pack_gate_up, whose device layout
+ * interleaves the halves: in each 128-column tile, per block of 16 columns,
+ * 8 gate columns and the 8 matching up columns (a gate column and its up
+ * column are then handled by lanes 8 apart of one warp).
+ *
+ *   x            bf16 [M][K], device;   y   bf16 [M][H], device
+ *   qweight_dev  u32 [K/8][2H], device (from w4a16_pack_gate_up)
+ *   H            columns of each half: a multiple of 64 (W4A16_EUNSUPPORTED)
+ *
+ * path, flags, workspace and errors as for w4a16_gemm_ex with N = 2H (the
+ * workspace is w4a16_workspace_bytes_path(path, M, 2H, K, group)).
+ */
+int w4a16_gemm_gate_up_silu(int path, unsigned flags, const void *x, const uint32_t *qweight_dev,
+                            const void *scales, const uint32_t *qzeros, int M, int H, int K,
+                            int group, void *y, void *workspace, size_t workspace_bytes,
+                            w4a16_stream_t stream);
+
+/* Canonical [K/8][2H] fused gate/up codes -> the interleaved device layout of
+ * w4a16_gemm_gate_up_silu (same size; H a multiple of 64), and its exact
+ * inverse.  Arguments and errors as for w4a16_pack / w4a16_unpack. */
+int w4a16_pack_gate_up(const uint32_t *qweight, uint32_t *qweight_dev, int K, int H,
+                       w4a16_stream_t stream);
+int w4a16_unpack_gate_up(const uint32_t *qweight_dev, uint32_t *qweight, int K, int H,
+                         w4a16_stream_t stream);
+
 /* Workspace bytes for a given path (0 if none); 0 for unsupported input. */
 size_t w4a16_workspace_bytes_path(int path, int M, int N, int K, int group);
 

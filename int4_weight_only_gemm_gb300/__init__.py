@@ -59,6 +59,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.w4a16_pack.argtypes = [vp, vp, ci, ci, vp]
             lib.w4a16_requant_pack.argtypes = [vp, vp, vp, ci, ci, ci, vp, vp]
             lib.w4a16_unpack.argtypes = [vp, vp, ci, ci, vp]
+            lib.w4a16_pack_gate_up.argtypes = [vp, vp, ci, ci, vp]
+            lib.w4a16_unpack_gate_up.argtypes = [vp, vp, ci, ci, vp]
+            lib.w4a16_gemm_gate_up_silu.argtypes = [ci, ctypes.c_uint, vp, vp, vp, vp, ci, ci, ci, ci, vp, vp, sz, vp]
             lib.w4a16_workspace_bytes.argtypes = [ci, ci, ci, ci]
             lib.w4a16_workspace_bytes.restype = sz
             lib.w4a16_workspace_bytes_max.argtypes = [ci, ci, ci, ci]
@@ -144,6 +147,64 @@ def w4a16_unpack(qweight_dev: torch.Tensor, out: torch.Tensor | None = None, str
     _check(out, "out", torch.int32, qweight_dev.shape)
     _raise(load_library().w4a16_unpack(qweight_dev.data_ptr(), out.data_ptr(), K, N, _stream(stream)),
            "w4a16_unpack")
+    return out
+
+
+def w4a16_pack_gate_up(qweight: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Canonical [K/8, 2H] int32 codes of fused gate/up weights (gate columns
+    first) -> the interleaved device layout of w4a16_gemm_gate_up_silu."""
+    _check(qweight, "qweight", torch.int32)
+    K, H = qweight.shape[0] * 8, qweight.shape[1] // 2
+    if out is None:
+        out = torch.empty_like(qweight)
+    _check(out, "out", torch.int32, qweight.shape)
+    _raise(load_library().w4a16_pack_gate_up(qweight.data_ptr(), out.data_ptr(), K, H, _stream(stream)),
+           "w4a16_pack_gate_up")
+    return out
+
+
+def w4a16_unpack_gate_up(qweight_dev: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Exact inverse of w4a16_pack_gate_up."""
+    _check(qweight_dev, "qweight_dev", torch.int32)
+    K, H = qweight_dev.shape[0] * 8, qweight_dev.shape[1] // 2
+    if out is None:
+        out = torch.empty_like(qweight_dev)
+    _check(out, "out", torch.int32, qweight_dev.shape)
+    _raise(load_library().w4a16_unpack_gate_up(qweight_dev.data_ptr(), out.data_ptr(), K, H, _stream(stream)),
+           "w4a16_unpack_gate_up")
+    return out
+
+
+def w4a16_gemm_gate_up_silu(x: torch.Tensor, qweight_dev: torch.Tensor, scales: torch.Tensor,
+                            qzeros: torch.Tensor, group: int = 128, out: torch.Tensor | None = None,
+                            workspace: torch.Tensor | None = None, path: int = PATH_AUTO, stream=None,
+                            flags: int | None = None) -> torch.Tensor:
+    """y = silu(x . Wg) * (x . Wu) in bf16 [M, H] for fused gate/up weights
+    [K, 2H] packed by w4a16_pack_gate_up (scales / qzeros canonical, [G, 2H]
+    and [G, 2H/8])."""
+    _check(x, "x", torch.bfloat16)
+    if x.dim() != 2:
+        raise ValueError("x must be [M, K]")
+    M, K = x.shape
+    N = qweight_dev.shape[1]
+    H = N // 2
+    G = K // group if group > 0 else 0
+    _check(qweight_dev, "qweight_dev", torch.int32, (K // 8, N))
+    _check(scales, "scales", torch.float16, (G, N))
+    _check(qzeros, "qzeros", torch.int32, (G, N // 8))
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    _check(out, "out", torch.bfloat16, (M, H))
+    lib = load_library()
+    need = int(lib.w4a16_workspace_bytes_path(path, M, N, K, group))
+    if workspace is None and need:
+        workspace = _cached_workspace(need, x.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.w4a16_gemm_gate_up_silu(path, FLAG_PDL if flags is None else flags, x.data_ptr(),
+                                     qweight_dev.data_ptr(), scales.data_ptr(), qzeros.data_ptr(), M, H, K, group,
+                                     out.data_ptr(), ws_ptr, ws_bytes, _stream(stream))
+    _raise(st, "w4a16_gemm_gate_up_silu")
     return out
 
 

@@ -51,8 +51,9 @@ int check_kn(int N, int K) {
     return W4A16_OK;
 }
 
+// ny: columns of y (N for the plain product, N / 2 for the fused gate/up one)
 int check_gemm(const void* x, const uint32_t* qd, const void* scales, const uint32_t* qzeros, int M, int N, int K,
-               int group, void* y) {
+               int group, void* y, int ny) {
     if (!x || !qd || !scales || !qzeros || !y) return W4A16_EINVAL;
     if (M < 1) return W4A16_EINVAL;
     if (group != 128) return W4A16_EUNSUPPORTED;
@@ -60,11 +61,32 @@ int check_gemm(const void* x, const uint32_t* qd, const void* scales, const uint
     if (st != W4A16_OK) return st;
     if (!aligned16(x) || !aligned16(qd) || !aligned16(y) || !aligned16(scales) || !aligned16(qzeros))
         return W4A16_EALIGN;
-    const size_t ybytes = (size_t)M * N * 2;
+    const size_t ybytes = (size_t)M * ny * 2;
     const int G = K / group;
     if (overlaps(y, ybytes, x, (size_t)M * K * 2) || overlaps(y, ybytes, qd, (size_t)K / 2 * N) ||
         overlaps(y, ybytes, scales, (size_t)G * N * 2) || overlaps(y, ybytes, qzeros, (size_t)G * N / 2))
         return W4A16_EINVAL;
+    return W4A16_OK;
+}
+
+// Fused gate/up weights: H = columns of each half, a multiple of 64 so that
+// every 128-column device tile holds 64 gate and 64 up columns.
+int check_gate_up(int H, int K) {
+    if (H < 64 || H % 64 != 0) return H < 1 ? W4A16_EINVAL : W4A16_EUNSUPPORTED;
+    if (H > (1 << 29)) return W4A16_EUNSUPPORTED;
+    return check_kn(2 * H, K);
+}
+
+int repack_gate_up(bool pack, const uint32_t* src, uint32_t* dst, int K, int H, cudaStream_t stream) {
+    if (!src || !dst) return W4A16_EINVAL;
+    int st = check_gate_up(H, K);
+    if (st != W4A16_OK) return st;
+    if (!aligned16(src) || !aligned16(dst)) return W4A16_EALIGN;
+    const size_t bytes = (size_t)K / 2 * (2 * (size_t)H);
+    if (overlaps(src, bytes, dst, bytes)) return W4A16_EINVAL;
+    const cudaError_t e = pack ? launch_pack(src, dst, K, 2 * H, H, stream) : launch_unpack(src, dst, K, 2 * H, H, stream);
+    if (e != cudaSuccess) return W4A16_ECUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return W4A16_OK;
 }
 
@@ -95,10 +117,11 @@ size_t ws_for_path(int path, int M, int N, int K, int sms) {
 constexpr unsigned kDefaultFlags = W4A16_FLAG_PDL;
 constexpr unsigned kKnownFlags = W4A16_FLAG_PDL | W4A16_FLAG_STATIC_WEIGHTS;
 
+// guH > 0: fused gate/up weights with N = 2 guH columns, y = silu(gate) * up of [M][guH]
 int run_gemm(int path, unsigned flags, const void* x, const uint32_t* qd, const void* scales, const uint32_t* qzeros,
-             int M, int N, int K, int group, void* y, void* ws, size_t ws_bytes, cudaStream_t stream) {
+             int M, int N, int K, int group, void* y, void* ws, size_t ws_bytes, cudaStream_t stream, int guH = 0) {
     if (flags & ~kKnownFlags) return W4A16_EINVAL;
-    int st = check_gemm(x, qd, scales, qzeros, M, N, K, group, y);
+    int st = check_gemm(x, qd, scales, qzeros, M, N, K, group, y, guH ? guH : N);
     if (st != W4A16_OK) return st;
     const int dev = current_device();
     if (dev < 0) return W4A16_ECUDA;
@@ -111,13 +134,13 @@ int run_gemm(int path, unsigned flags, const void* x, const uint32_t* qd, const 
         if (!gemv_plan(M, N, K, sms, &gp)) return W4A16_EUNSUPPORTED;
         if (gp.ws_bytes && (!ws || ws_bytes < gp.ws_bytes || !aligned16(ws))) return W4A16_EWORKSPACE;
         e = launch_gemv(static_cast<const uint16_t*>(x), qd, static_cast<const uint16_t*>(scales), qzeros,
-                        static_cast<uint16_t*>(y), M, N, K, ws, gp, stream, flags);
+                        static_cast<uint16_t*>(y), M, N, K, ws, gp, stream, flags, guH);
     } else if (path == W4A16_PATH_TC) {
         TcPlan tp;
         if (!tc_plan(M, N, K, sms, &tp)) return W4A16_EUNSUPPORTED;
         if (tp.ws_bytes && (!ws || ws_bytes < tp.ws_bytes || !aligned16(ws))) return W4A16_EWORKSPACE;
         e = launch_tc(static_cast<const uint16_t*>(x), qd, static_cast<const uint16_t*>(scales), qzeros,
-                      static_cast<uint16_t*>(y), M, N, K, ws, tp, stream, flags);
+                      static_cast<uint16_t*>(y), M, N, K, ws, tp, stream, flags, guH);
     } else {
         return W4A16_EINVAL;
     }
@@ -140,7 +163,7 @@ int w4a16_pack(const uint32_t* qweight, uint32_t* qweight_dev, int K, int N, w4a
     if (!aligned16(qweight) || !aligned16(qweight_dev)) return W4A16_EALIGN;
     const size_t bytes = (size_t)K / 2 * N;
     if (overlaps(qweight, bytes, qweight_dev, bytes)) return W4A16_EINVAL;
-    if (launch_pack(qweight, qweight_dev, K, N, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (launch_pack(qweight, qweight_dev, K, N, 0, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return W4A16_ECUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return W4A16_OK;
@@ -153,10 +176,28 @@ int w4a16_unpack(const uint32_t* qweight_dev, uint32_t* qweight, int K, int N, w
     if (!aligned16(qweight) || !aligned16(qweight_dev)) return W4A16_EALIGN;
     const size_t bytes = (size_t)K / 2 * N;
     if (overlaps(qweight, bytes, qweight_dev, bytes)) return W4A16_EINVAL;
-    if (launch_unpack(qweight_dev, qweight, K, N, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (launch_unpack(qweight_dev, qweight, K, N, 0, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return W4A16_ECUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return W4A16_OK;
+}
+
+int w4a16_pack_gate_up(const uint32_t* qweight, uint32_t* qweight_dev, int K, int H, w4a16_stream_t stream) {
+    return repack_gate_up(true, qweight, qweight_dev, K, H, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int w4a16_unpack_gate_up(const uint32_t* qweight_dev, uint32_t* qweight, int K, int H, w4a16_stream_t stream) {
+    return repack_gate_up(false, qweight_dev, qweight, K, H, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int w4a16_gemm_gate_up_silu(int path, unsigned flags, const void* x, const uint32_t* qweight_dev, const void* scales,
+                            const uint32_t* qzeros, int M, int H, int K, int group, void* y, void* workspace,
+                            size_t workspace_bytes, w4a16_stream_t stream) {
+    if (H < 1) return W4A16_EINVAL;
+    const int st = check_gate_up(H, K);
+    if (st != W4A16_OK) return st;
+    return run_gemm(path, flags, x, qweight_dev, scales, qzeros, M, 2 * H, K, group, y, workspace, workspace_bytes,
+                    reinterpret_cast<cudaStream_t>(stream), H);
 }
 
 int w4a16_requant_pack(const void* w, const void* scales, const uint32_t* qzeros, int K, int N, int group,

@@ -71,6 +71,7 @@ struct TcParams {
     int splits;      // units from `whole` on: each later tile in `splits` K pieces
     int units;       // whole + (tiles - whole) * splits
     int prefetch;    // weights may be loaded before the preceding grid completes
+    int guH;         // > 0: fused gate/up weights (N = 2 guH); y[M][guH] = silu(gate) * up
 };
 
 // Configuration per token-tile width NT (one CTA per SM).
@@ -228,7 +229,8 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
             // them with 4-byte async copies.
             int q = 0, issued = 0;
             bool ok = true;
-            const bool zbulk = p.N % 32 == 0;
+            // (fused gate/up weights: a tile's zero words come from two places)
+            const bool zbulk = !p.guH && p.N % 32 == 0;
             // This warp touches only weights and zeros: with static weights it
             // never waits on the preceding grid, otherwise once before any load.
             if (!p.prefetch) pdl_wait();
@@ -248,7 +250,10 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                     if (ok) {
                         if (lane == 0) {
                             if (!zbulk) {
-                                for (int i = 0; i < W / 8; ++i) cp_async_4(smem + C::kZOff + s * 64 + i * 4, zsrc + i);
+                                for (int i = 0; i < W / 8; ++i) {
+                                    const int zi = p.guH ? (gu_column(128 * ui.nb + 8 * i, p.guH) >> 3) - 16 * ui.nb : i;
+                                    cp_async_4(smem + C::kZOff + s * 64 + i * 4, zsrc + zi);
+                                }
                                 cp_async_mbar_arrive(&full[s]);
                             }
                             mbar_arrive_expect_tx(&full[s], wbytes + zbytes);
@@ -421,7 +426,8 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
             if (lq_u < p.units) {
                 const int W = L.width(lq_nb);
                 const int tc = (t < W ? t : W - 1) & ~1;
-                cp_async_4(sring + slot * 128 * R, p.scales + (size_t)lq_g * p.N + 128 * lq_nb + tc);
+                const int col = 128 * lq_nb + tc;  // even: the pair (col, col + 1) is canonical-adjacent too
+                cp_async_4(sring + slot * 128 * R, p.scales + (size_t)lq_g * p.N + (p.guH ? gu_column(col, p.guH) : col));
                 ++lq_g;
             }
             cp_async_commit();  // possibly empty: keeps one group per slot
@@ -490,7 +496,17 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
             const int tok0 = ui.mb * NT + r * CW;
             if (all_ok) {
                 if (ui.ns == 1) {
-                    if (t < W) {
+                    if (p.guH) {
+                        // thread t (t % 16 < 8) holds a gate column, thread t + 8 its up column
+                        const size_t col = (size_t)gu_column(n, p.guH);
+#pragma unroll
+                        for (int j = 0; j < CW; ++j) {
+                            const float g = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
+                            const float u = __shfl_xor_sync(0xFFFFFFFFu, g, 8);
+                            if (!(t & 8) && tok0 + j < p.M)
+                                p.y[(size_t)(tok0 + j) * p.guH + col] = f32_to_bf16_rn(silu_mul(g, u));
+                        }
+                    } else if (t < W) {
 #pragma unroll
                         for (int j = 0; j < CW; ++j)
                             if (tok0 + j < p.M)
@@ -538,7 +554,17 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                                     sum[j].w += v.w;
                                 }
                             }
-                            if (t < W) {
+                            if (p.guH) {
+                                const size_t col = (size_t)gu_column(n, p.guH);
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) {
+                                    const float4& v = sum[j / 4];
+                                    const float g = (j & 3) == 0 ? v.x : (j & 3) == 1 ? v.y : (j & 3) == 2 ? v.z : v.w;
+                                    const float u = __shfl_xor_sync(0xFFFFFFFFu, g, 8);
+                                    if (!(t & 8) && j0 + j < CW && tok0 + j0 + j < p.M)
+                                        p.y[(size_t)(tok0 + j0 + j) * p.guH + col] = f32_to_bf16_rn(silu_mul(g, u));
+                                }
+                            } else if (t < W) {
 #pragma unroll
                                 for (int j = 0; j < 16; ++j) {
                                     const float4& v = sum[j / 4];
@@ -677,7 +703,7 @@ static cudaError_t launch_nt(const CUtensorMap& tm, const TcParams& prm, const T
 
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
                       uint16_t* y, int M, int N, int K, void* ws, const TcPlan& plan, cudaStream_t s,
-                      unsigned flags) {
+                      unsigned flags, int guH) {
     auto encode = get_encode();
     if (!encode) return cudaErrorNotSupported;
     CUtensorMap tm;
@@ -710,6 +736,7 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
     prm.units = plan.units;
     const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
+    prm.guH = guH;
     switch (plan.NT) {
         case 16: return launch_nt<16>(tm, prm, plan, s, pdl);
         case 32: return launch_nt<32>(tm, prm, plan, s, pdl);

@@ -60,6 +60,7 @@ struct GemvParams {
     int base, extra;  // split: tile t has base + (t < extra) pieces; CTAs are numbered tile by tile
     int S;          // ring stages
     int prefetch;   // weights may be loaded before the preceding grid completes
+    int guH;        // > 0: fused gate/up weights (N = 2 guH); y[M][guH] = silu(gate) * up
 };
 
 constexpr int kGemvConsumerWarps = 16;                       // four warpgroups
@@ -272,8 +273,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
             const int Wp = L.width(pnb);
             const int tp = t < Wp ? t : Wp - 1;
             const int n = 128 * pnb + tp;
-            sc = __ldg(p.scales + (size_t)pkb * p.N + n);
-            zw = __ldg(p.qzeros + (size_t)pkb * (p.N / 8) + (n >> 3));
+            const int cn = p.guH ? gu_column(n, p.guH) : n;  // canonical column of the scale and zero
+            sc = __ldg(p.scales + (size_t)pkb * p.N + cn);
+            zw = __ldg(p.qzeros + (size_t)pkb * (p.N / 8) + (cn >> 3));
         }
         pv += 4;
         pkb += 4;
@@ -379,7 +381,14 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
                 const float v = ((red[(0 * M + m) * 128 + t] + red[(1 * M + m) * 128 + t]) +
                                  red[(2 * M + m) * 128 + t]) + red[(3 * M + m) * 128 + t];
                 if (whole) {
-                    if (t < W && m < p.M) p.y[(size_t)m * p.N + n] = f32_to_bf16_rn(v);
+                    if (p.guH) {
+                        // thread t (t % 16 < 8) holds a gate column, thread t + 8 its up column
+                        const float u = __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+                        if (!(t & 8) && m < p.M)
+                            p.y[(size_t)m * p.guH + gu_column(n, p.guH)] = f32_to_bf16_rn(silu_mul(v, u));
+                    } else if (t < W && m < p.M) {
+                        p.y[(size_t)m * p.N + n] = f32_to_bf16_rn(v);
+                    }
                 } else {
                     p.partials[((size_t)blockIdx.x * M + m) * 128 + t] = v;  // one partial per CTA
                 }
@@ -416,7 +425,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
                             for (int i = 0; i < kBatch; ++i)
                                 if (c0 + i <= cl) sum += v[i];
                         }
-                        if (t < W && m < p.M) p.y[(size_t)m * p.N + n] = f32_to_bf16_rn(sum);
+                        if (p.guH) {
+                            const float u = __shfl_xor_sync(0xFFFFFFFFu, sum, 8);
+                            if (!(t & 8) && m < p.M)
+                                p.y[(size_t)m * p.guH + gu_column(n, p.guH)] = f32_to_bf16_rn(silu_mul(sum, u));
+                        } else if (t < W && m < p.M) {
+                            p.y[(size_t)m * p.N + n] = f32_to_bf16_rn(sum);
+                        }
                     }
                     if (ct == 0) p.counters[nb] = 0u;
                 }
@@ -503,7 +518,7 @@ static cudaError_t launch_m(const GemvParams& prm, const GemvPlan& plan, cudaStr
 
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
                         uint16_t* y, int M, int N, int K, void* ws, const GemvPlan& plan, cudaStream_t s,
-                        unsigned flags) {
+                        unsigned flags, int guH) {
     const Layout L(K, N);
     GemvParams prm;
     prm.x = x;
@@ -524,6 +539,7 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qd, const uint16_t* s
     prm.S = plan.S;
     const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
+    prm.guH = guH;
     switch (gemv_mtile(M)) {
         case 1: return launch_m<1>(prm, plan, s, pdl);
         case 2: return launch_m<2>(prm, plan, s, pdl);

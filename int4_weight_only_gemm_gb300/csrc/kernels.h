@@ -9,8 +9,22 @@
 
 namespace w4a16 {
 
-cudaError_t launch_pack(const uint32_t* q, uint32_t* qd, int K, int N, cudaStream_t s);
-cudaError_t launch_unpack(const uint32_t* qd, uint32_t* q, int K, int N, cudaStream_t s);
+// Fused gate/up weights [K][2H] (gate columns 0..H-1, up columns H..2H-1) in
+// the device layout: column j of 128-column device tile t holds gate column
+// 64t + 8b + r when j % 16 < 8 and up column H + 64t + 8b + r otherwise
+// (b = j / 16, r = j % 8), so a gate column and its up column sit 8 apart in
+// one warp.  Returns the canonical column of device column n.
+__host__ __device__ inline int gu_column(int n, int H) {
+    const int t = n >> 7, j = n & 127;
+    return ((j & 8) ? H : 0) + 64 * t + 8 * (j >> 4) + (j & 7);
+}
+
+// silu(g) * u = g / (1 + e^-g) * u, in f32
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+// guH = 0: plain layout; guH = H: fused gate/up weights with N = 2H columns
+cudaError_t launch_pack(const uint32_t* q, uint32_t* qd, int K, int N, int guH, cudaStream_t s);
+cudaError_t launch_unpack(const uint32_t* qd, uint32_t* q, int K, int N, int guH, cudaStream_t s);
 cudaError_t launch_requant_pack(const uint16_t* w, const uint16_t* scales, const uint32_t* qzeros, uint32_t* qd,
                                 int K, int N, cudaStream_t s);
 
@@ -23,9 +37,10 @@ struct GemvPlan {
     size_t smem, ws_bytes;
 };
 bool gemv_plan(int M, int N, int K, int sms, GemvPlan* out);
+// guH > 0: fused gate/up weights (N = 2 guH), y is [M][guH] = silu(gate) * up
 cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
                         uint16_t* y, int M, int N, int K, void* ws, const GemvPlan& plan, cudaStream_t s,
-                        unsigned flags);
+                        unsigned flags, int guH);
 int gemv_read_status();
 
 // tcgen05 tensor-core GEMM (any M)
@@ -39,7 +54,7 @@ struct TcPlan {
 bool tc_plan(int M, int N, int K, int sms, TcPlan* out);
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
                       uint16_t* y, int M, int N, int K, void* ws, const TcPlan& plan, cudaStream_t s,
-                      unsigned flags);
+                      unsigned flags, int guH);
 
 // Launch `kern` with an optional programmatic-stream-serialization attribute.
 template <typename Kern, typename... Args>

@@ -93,7 +93,7 @@ extern "C" int w4a16_gemm_noalloc(const void* x, const uint32_t* qweight_dev, co
     const size_t ntiles = (size_t)(N + 127) / 128;
     if (cudaMemsetAsync(scratch, 0, ntiles * sizeof(uint32_t), s) != cudaSuccess) return W4A16_ECUDA;
     if (launch_gemv(static_cast<const uint16_t*>(x), qweight_dev, static_cast<const uint16_t*>(scales), qzeros,
-                    static_cast<uint16_t*>(y), M, N, K, scratch, plan, s, 0u) != cudaSuccess)
+                    static_cast<uint16_t*>(y), M, N, K, scratch, plan, s, 0u, 0) != cudaSuccess)
         return W4A16_ECUDA;
     return W4A16_OK;
 }

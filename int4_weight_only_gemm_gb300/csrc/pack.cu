@@ -27,13 +27,13 @@ __device__ __forceinline__ void decode_dev_word(const Layout& L, size_t d, int& 
     kw = 16 * kb + 4 * c + j;
 }
 
-__global__ void pack_kernel(const uint32_t* __restrict__ q, uint32_t* __restrict__ qd, int K, int N) {
+__global__ void pack_kernel(const uint32_t* __restrict__ q, uint32_t* __restrict__ qd, int K, int N, int guH) {
     const Layout L(K, N);
     const size_t total = (size_t)(K / 8) * N;
     for (size_t d = blockIdx.x * (size_t)blockDim.x + threadIdx.x; d < total; d += (size_t)gridDim.x * blockDim.x) {
         int n, kw;
         decode_dev_word(L, d, n, kw);
-        const uint32_t w = q[(size_t)kw * N + n];
+        const uint32_t w = q[(size_t)kw * N + (guH ? gu_column(n, guH) : n)];
         uint32_t o = 0;
 #pragma unroll
         for (int r = 0; r < 8; ++r) o |= ((w >> (4 * r)) & 0xFu) << (4 * dev_nibble_pos(r));
@@ -41,7 +41,7 @@ __global__ void pack_kernel(const uint32_t* __restrict__ q, uint32_t* __restrict
     }
 }
 
-__global__ void unpack_kernel(const uint32_t* __restrict__ qd, uint32_t* __restrict__ q, int K, int N) {
+__global__ void unpack_kernel(const uint32_t* __restrict__ qd, uint32_t* __restrict__ q, int K, int N, int guH) {
     const Layout L(K, N);
     const size_t total = (size_t)(K / 8) * N;
     for (size_t d = blockIdx.x * (size_t)blockDim.x + threadIdx.x; d < total; d += (size_t)gridDim.x * blockDim.x) {
@@ -51,7 +51,7 @@ __global__ void unpack_kernel(const uint32_t* __restrict__ qd, uint32_t* __restr
         uint32_t w = 0;
 #pragma unroll
         for (int r = 0; r < 8; ++r) w |= ((o >> (4 * dev_nibble_pos(r))) & 0xFu) << (4 * r);
-        q[(size_t)kw * N + n] = w;
+        q[(size_t)kw * N + (guH ? gu_column(n, guH) : n)] = w;
     }
 }
 
@@ -60,13 +60,13 @@ static int grid_for(size_t total) {
     return (int)(b > 65535 ? 65535 : (b == 0 ? 1 : b));
 }
 
-cudaError_t launch_pack(const uint32_t* q, uint32_t* qd, int K, int N, cudaStream_t s) {
-    pack_kernel<<<grid_for((size_t)(K / 8) * N), 256, 0, s>>>(q, qd, K, N);
+cudaError_t launch_pack(const uint32_t* q, uint32_t* qd, int K, int N, int guH, cudaStream_t s) {
+    pack_kernel<<<grid_for((size_t)(K / 8) * N), 256, 0, s>>>(q, qd, K, N, guH);
     return cudaGetLastError();
 }
 
-cudaError_t launch_unpack(const uint32_t* qd, uint32_t* q, int K, int N, cudaStream_t s) {
-    unpack_kernel<<<grid_for((size_t)(K / 8) * N), 256, 0, s>>>(qd, q, K, N);
+cudaError_t launch_unpack(const uint32_t* qd, uint32_t* q, int K, int N, int guH, cudaStream_t s) {
+    unpack_kernel<<<grid_for((size_t)(K / 8) * N), 256, 0, s>>>(qd, q, K, N, guH);
     return cudaGetLastError();
 }
 

@@ -259,3 +259,55 @@ def requant_codes(w, scales, qzeros, group: int = 128) -> np.ndarray:
     c = np.clip(r + z[gi, :], 0.0, 15.0)
     assert c.shape == (K, N) and G * group == K
     return c.astype(np.uint8)
+
+
+# ---- fused gate/up projection with the SiLU-multiply epilogue ----------------
+#
+# A gated MLP's gate and up projections stored as one weight matrix [K][2H]
+# (gate columns 0..H-1, up columns H..2H-1) on one quantization grid, followed
+# by y = silu(g) * u.  The pages name the fused gate/up shape of the decoder
+# (2560 x 19456) but not the activation; the plain reading of a gated MLP is
+# the one taken: silu(g) = g / (1 + exp(-g)) = g * logistic(g), applied to the
+# exact products, so nothing is rounded before the final result.
+
+def silu_mul(y: np.ndarray, H: int) -> np.ndarray:
+    """y[:, :H] = gate pre-activations g, y[:, H:] = up values u -> g / (1 + e^-g) * u (fp64)."""
+    y = np.asarray(y, dtype=np.float64)
+    assert y.shape[-1] == 2 * H
+    g, u = y[..., :H], y[..., H:]
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g)) * u
+
+
+def gemm_gate_up_silu(x, qweight, scales, qzeros, H: int, group: int = 128) -> np.ndarray:
+    """Full silu(x . Wg) * (x . Wu) [M][H] in fp64: the triple-loop GEMM, then silu_mul."""
+    return silu_mul(gemm(x, qweight, scales, qzeros, group), H)
+
+
+def gemm_gate_up_silu_elems(x, qweight, scales, qzeros, H: int, ms, hs, group: int = 128) -> np.ndarray:
+    """Selected outputs [ms[i]][hs[i]]: the gate and up products one by one, then silu * up."""
+    ms = np.asarray(ms, dtype=np.int64)
+    hs = np.asarray(hs, dtype=np.int64)
+    g = gemm_elems(x, qweight, scales, qzeros, ms, hs, group)
+    u = gemm_elems(x, qweight, scales, qzeros, ms, hs + H, group)
+    return silu_mul(np.stack([g, u], axis=-1).reshape(-1, 2), 1).reshape(g.shape)
+
+
+def gate_up_device_columns(H: int) -> np.ndarray:
+    """canonical[d]: the canonical column held by device column d of the fused
+    layout.  Each 128-column tile t holds 64 gate and 64 up columns; within the
+    tile, block b of 16 columns holds gate columns 64t + 8b .. +7, then the up
+    columns H + 64t + 8b .. +7."""
+    d = np.arange(2 * H)
+    t, j = d // 128, d % 128
+    b, r = j // 16, j % 16
+    return np.where(r < 8, 64 * t + 8 * b + r, H + 64 * t + 8 * b + (r - 8))
+
+
+def device_layout_gate_up(qweight: np.ndarray, H: int) -> np.ndarray:
+    """Canonical fused words [K/8][2H] -> device layout: the columns put in the
+    interleaved order, then the plain tiled device layout."""
+    qweight = _c(qweight, np.uint32)
+    if H % 64 or qweight.shape[1] != 2 * H:
+        raise ValueError("fused gate/up layout needs N = 2H with H % 64 == 0")
+    return device_layout(np.ascontiguousarray(qweight[:, gate_up_device_columns(H)]))
