@@ -398,6 +398,68 @@ def measure_requant(w, torch, device, hbm, reps=200):
             "bytes": nbytes, "shape": f"{K}x{N}", "launch": "stream loop of launches (no graph)"}
 
 
+def measure_gate_up_silu(w, torch, device, hbm, bf16_peak):
+    """The fused gate/up projection with its SiLU-multiply epilogue on the
+    decoder's 2560 x 19456 shape (H = 9728) at M = 1, 16 and 2048, beside the
+    plain gate_up GEMM of the same weights: CUDA graphs over rotating weight
+    copies (> L2), as for the decode step."""
+    K, N = wi.shape_kn("gate_up")
+    H = N // 2
+    out = {}
+    for M, copies, n, seed in ((1, COPIES, 2000, 1), (16, COPIES, 2000, 2), (2048, 2, 20, 3)):
+        p = wi.generate(M, K, N, seed=seed, shape_index=2)
+        x, qw, sc, qz = w.to_device(p, device)
+        fused = [w.w4a16_pack_gate_up(qw) for _ in range(copies)]
+        plain = [w.w4a16_pack(qw) for _ in range(copies)]
+        del qw
+        ws = w.new_workspace(w.w4a16_workspace_bytes(M, N, K), device)
+        y_f = torch.empty((M, H), dtype=torch.bfloat16, device=device)
+        y_p = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        res = {}
+        for name, qds, call in (
+                ("fused", fused, lambda qd: w.w4a16_gemm_gate_up_silu(x, qd, sc, qz, out=y_f, workspace=ws)),
+                ("plain", plain, lambda qd: w.w4a16_gemm(x, qd, sc, qz, out=y_p, workspace=ws))):
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                for qd in qds:
+                    call(qd)
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for qd in qds:
+                    call(qd)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            reps = max(1, n // copies)
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            res[name] = e0.elapsed_time(e1) * 1e3 / (reps * copies)
+            del g
+        G = K // 128
+        fbytes = K * N // 2 + G * N * 2 + G * N // 2 + M * K * 2 + M * H * 2
+        entry = {"us": res["fused"], "plain_gate_up_us": res["plain"], "GB/s": fbytes / res["fused"] / 1e3}
+        if M <= 16:
+            entry["frac"] = entry["GB/s"] / hbm
+        else:
+            entry["TFLOP/s"] = gemm_flops(M, K, N) / res["fused"] / 1e6
+            entry["frac"] = entry["TFLOP/s"] / bf16_peak
+        # a separate activation pass would write y [M][2H] in bf16 and read it back
+        entry["intermediate_bytes_avoided"] = M * N * 2 * 2 - M * H * 2
+        out[f"M={M}"] = entry
+        del x, sc, qz, fused, plain, ws, y_f, y_p
+        torch.cuda.empty_cache()
+    out["shape"] = f"K={K}, 2H={N} (H={H})"
+    return out
+
+
 def run_case(case, reps):
     """One seeded GEMM of the named layer shape, launched `reps` times back to
     back on the current stream (the workload of the ncu summaries)."""
@@ -530,6 +592,7 @@ def main():
 
     if rank == 0 and not args.no_extra:
         extra["requant_pack_gate_up"] = measure_requant(w, torch, device, hbm)
+        extra["gate_up_silu"] = measure_gate_up_silu(w, torch, device, hbm, bf16_peak)
 
     e2e = None
     if not args.no_e2e:

@@ -248,14 +248,13 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                         !mbar_wait_warp(&done[(q - SS) % ND], ((q - SS) / ND) & 1, abort_flag, &g_tc_status))
                         ok = false;
                     if (ok) {
+                        if (!zbulk && lane < W / 8) {  // one zero word per lane
+                            const int zi = p.guH ? (gu_column(128 * ui.nb + 8 * lane, p.guH) >> 3) - 16 * ui.nb : lane;
+                            cp_async_4(smem + C::kZOff + s * 64 + lane * 4, zsrc + zi);
+                            cp_async_mbar_arrive(&full[s]);
+                        }
+                        __syncwarp();  // every lane's pending arrival precedes the expected-bytes arrival
                         if (lane == 0) {
-                            if (!zbulk) {
-                                for (int i = 0; i < W / 8; ++i) {
-                                    const int zi = p.guH ? (gu_column(128 * ui.nb + 8 * i, p.guH) >> 3) - 16 * ui.nb : i;
-                                    cp_async_4(smem + C::kZOff + s * 64 + i * 4, zsrc + zi);
-                                }
-                                cp_async_mbar_arrive(&full[s]);
-                            }
                             mbar_arrive_expect_tx(&full[s], wbytes + zbytes);
                             bulk_g2s(smem + C::kPOff + s * 8192, wsrc, wbytes, &full[s]);
                             if (zbulk) bulk_g2s(smem + C::kZOff + s * 64, zsrc, zbytes, &full[s]);
@@ -497,14 +496,18 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
             if (all_ok) {
                 if (ui.ns == 1) {
                     if (p.guH) {
-                        // thread t (t % 16 < 8) holds a gate column, thread t + 8 its up column
-                        const size_t col = (size_t)gu_column(n, p.guH);
+                        // Thread t (t % 16 < 8) holds a gate column, thread t + 8 its
+                        // up column.  Per pair of tokens one value crosses each way: the
+                        // gate lane finishes token j, the up lane token j + 1.
+                        const bool gate = !(t & 8);
+                        const size_t col = (size_t)gu_column(gate ? n : n - 8, p.guH);
 #pragma unroll
-                        for (int j = 0; j < CW; ++j) {
-                            const float g = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
-                            const float u = __shfl_xor_sync(0xFFFFFFFFu, g, 8);
-                            if (!(t & 8) && tok0 + j < p.M)
-                                p.y[(size_t)(tok0 + j) * p.guH + col] = f32_to_bf16_rn(silu_mul(g, u));
+                        for (int j = 0; j < CW; j += 2) {
+                            const float a0 = acc[j / 2].x, a1 = acc[j / 2].y;  // tokens j, j + 1
+                            const float r = __shfl_xor_sync(0xFFFFFFFFu, gate ? a1 : a0, 8);
+                            const int tok = tok0 + j + (gate ? 0 : 1);
+                            if (tok < p.M)
+                                p.y[(size_t)tok * p.guH + col] = f32_to_bf16_rn(gate ? silu_mul(a0, r) : silu_mul(r, a1));
                         }
                     } else if (t < W) {
 #pragma unroll
@@ -555,14 +558,17 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                                 }
                             }
                             if (p.guH) {
-                                const size_t col = (size_t)gu_column(n, p.guH);
+                                const bool gate = !(t & 8);
+                                const size_t col = (size_t)gu_column(gate ? n : n - 8, p.guH);
 #pragma unroll
-                                for (int j = 0; j < 16; ++j) {
+                                for (int j = 0; j < 16; j += 2) {
                                     const float4& v = sum[j / 4];
-                                    const float g = (j & 3) == 0 ? v.x : (j & 3) == 1 ? v.y : (j & 3) == 2 ? v.z : v.w;
-                                    const float u = __shfl_xor_sync(0xFFFFFFFFu, g, 8);
-                                    if (!(t & 8) && j0 + j < CW && tok0 + j0 + j < p.M)
-                                        p.y[(size_t)(tok0 + j0 + j) * p.guH + col] = f32_to_bf16_rn(silu_mul(g, u));
+                                    const float a0 = (j & 2) ? v.z : v.x, a1 = (j & 2) ? v.w : v.y;
+                                    const float r = __shfl_xor_sync(0xFFFFFFFFu, gate ? a1 : a0, 8);
+                                    const int jj = j0 + j + (gate ? 0 : 1);
+                                    if (jj < CW && tok0 + jj < p.M)
+                                        p.y[(size_t)(tok0 + jj) * p.guH + col] =
+                                            f32_to_bf16_rn(gate ? silu_mul(a0, r) : silu_mul(r, a1));
                                 }
                             } else if (t < W) {
 #pragma unroll
