@@ -593,6 +593,21 @@ def main():
     if rank == 0 and not args.no_extra:
         extra["requant_pack_gate_up"] = measure_requant(w, torch, device, hbm)
         extra["gate_up_silu"] = measure_gate_up_silu(w, torch, device, hbm, bf16_peak)
+        # batched speculative verify: b draft blocks of 16 tokens through the
+        # four projections of the layer, PDL-chained in one graph per step
+        vb = {}
+        for b in (1, 2, 3, 4):
+            M = 16 * b
+            wl3 = Workload(w, torch, [(s, M) for s in wi.LAYER], 2, COPIES, device)
+            ps, rt = wl3.graphs()
+            n = 2000
+            t_ms = time_graph_steps(torch, ps, rt, COPIES, n, 10)
+            us = t_ms / n * 1e3
+            vb[f"M={M}"] = {"us_per_step": us, "GB/s": wl3.bytes / us / 1e3, "frac": wl3.bytes / us / 1e3 / hbm,
+                            "tokens/s": M / us * 1e6}
+            del wl3, ps, rt
+            torch.cuda.empty_cache()
+        extra["verify_batched"] = vb
 
     e2e = None
     if not args.no_e2e:

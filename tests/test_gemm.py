@@ -87,7 +87,7 @@ def test_sweep_small_m_both_paths(M, shape):
         check_close(bf16_to_f64(d.run(path)), ref, f"sweep {shape} M={M} path={path}")
 
 
-@pytest.mark.parametrize("M", [16, 32])
+@pytest.mark.parametrize("M", [16, 32, 48])  # 48: three 16-token draft blocks verified together
 @pytest.mark.parametrize("shape", wi.LAYER)
 def test_sweep_mid_m_full(M, shape):
     p = wi.generate_named(shape, M, 4)
