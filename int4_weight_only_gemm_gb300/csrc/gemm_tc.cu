@@ -77,16 +77,16 @@ struct TcParams {
 // Configuration per token-tile width NT (one CTA per SM).
 template <int NT>
 struct TcCfg {
-    static constexpr int R = NT >= 128 ? 2 : 1;          // rescale warpgroups, each owning NT/R columns
-    static constexpr int SS = NT <= 16 ? 12 : NT <= 32 ? 10 : NT <= 128 ? 4 : 3;  // shared-memory ring stages
-    static constexpr int SA = NT <= 32 ? 4 : NT <= 128 ? 3 : 2;  // A buffers in tensor memory (q % SA)
+    static constexpr int R = NT >= 64 ? 2 : 1;           // rescale warpgroups, each owning NT/R columns
+    static constexpr int SS = NT <= 16 ? 12 : NT <= 32 ? 10 : NT <= 64 ? 8 : NT <= 128 ? 4 : 3;  // shared-memory ring stages
+    static constexpr int SA = NT <= 64 ? 4 : NT <= 128 ? 3 : 2;  // A buffers in tensor memory (q % SA)
     static constexpr int NDB = ((512 - SA * 64) / NT) < 8 ? ((512 - SA * 64) / NT) : 8;  // D accumulator ring
     static constexpr int kDone = 16;                     // ring of "MMAs of group q done" barriers
     // ring of "group q may be issued" barriers: its A buffer written and its D
     // buffer read out (arrivals for q follow the completion of q - SA and of
     // q - NDB, so max(SA, NDB) slots keep the phases apart)
     static constexpr int kReady = SA > NDB ? SA : NDB;
-    static constexpr int kDeqWG = NT <= 32 ? 4 : 2;      // dequant warpgroups, taking groups q % kDeqWG
+    static constexpr int kDeqWG = NT <= 64 ? 4 : 2;      // dequant warpgroups, taking groups q % kDeqWG
     static constexpr int kDeqWarps = 4 * kDeqWG;
     static constexpr int kResWarp0 = kDeqWarps;          // rescale warpgroups follow
     static constexpr int kMmaWarp = kDeqWarps + 4 * R;   // then the MMA warp (the only tcgen05.mma issuer)
@@ -518,11 +518,12 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                     }
                 } else {
                     const int tile = ui.ptile;  // counters and partials of the split tiles only
-                    // partial sums: [split tile][piece][column t][NT tokens], this warpgroup's CW tokens
-                    float4* part = reinterpret_cast<float4*>(p.partials + (((size_t)tile * ui.ns + ui.split) * 128 + t) * NT + r * CW);
+                    // partial sums: [split tile][piece][NT tokens][128 columns], so that a
+                    // warp writes (and the reduction reads) 32 adjacent columns at once;
+                    // this warpgroup's CW tokens
+                    float* part = p.partials + (((size_t)tile * ui.ns + ui.split) * NT + r * CW) * 128 + t;
 #pragma unroll
-                    for (int j = 0; j < CW; j += 4)
-                        part[j / 4] = make_float4(acc[j / 2].x, acc[j / 2].y, acc[j / 2 + 1].x, acc[j / 2 + 1].y);
+                    for (int j = 0; j < CW; ++j) part[(size_t)j * 128] = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
                     // hand-off: the barrier orders the warpgroups' partial stores
                     // before one thread, whose gpu-scope fence publishes them
                     // with its arrival; the last arrival fences again before
@@ -539,24 +540,21 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                     if (*sh_last) {
                         // every split's values for this thread, summed in split order,
                         // 16 tokens at a time
-                        const float4* base = reinterpret_cast<const float4*>(p.partials + ((size_t)tile * ui.ns * 128 + t) * NT + r * CW);
-                        const size_t sstride = (size_t)128 * NT / 4;  // float4s between splits
+                        const float* base = p.partials + ((size_t)tile * ui.ns * NT + r * CW) * 128 + t;
+                        const size_t sstride = (size_t)128 * NT;  // floats between splits
 #pragma unroll 1
                         for (int j0 = 0; j0 < CW; j0 += 16) {
-                            float4 sum[4];
+                            float sv[16];
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) sum[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+                            for (int j = 0; j < 16; ++j) sv[j] = 0.f;
+#pragma unroll 2
                             for (int sp = 0; sp < ui.ns; ++sp) {
 #pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    const float4 v = __ldcg(base + sp * sstride + j0 / 4 + j);
-                                    sum[j].x += v.x;
-                                    sum[j].y += v.y;
-                                    sum[j].z += v.z;
-                                    sum[j].w += v.w;
-                                }
+                                for (int j = 0; j < 16; ++j) sv[j] += __ldcg(base + sp * sstride + (size_t)(j0 + j) * 128);
                             }
+                            const float4 sum[4] = {make_float4(sv[0], sv[1], sv[2], sv[3]), make_float4(sv[4], sv[5], sv[6], sv[7]),
+                                                   make_float4(sv[8], sv[9], sv[10], sv[11]),
+                                                   make_float4(sv[12], sv[13], sv[14], sv[15])};
                             if (p.guH) {
                                 const bool gate = !(t & 8);
                                 const size_t col = (size_t)gu_column(gate ? n : n - 8, p.guH);
@@ -607,7 +605,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
 // so large M takes 192-token tiles: two D buffers of 192 columns still fit
 // beside two A buffers in the 512 tensor-memory columns.  Up to 256 tokens
 // the shorter per-group chain of 128-token tiles measured faster.
-static int tc_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 256 ? 128 : 192; }
+static int tc_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 256 ? 128 : 192; }
 
 bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
     const Layout L(K, N);
@@ -658,6 +656,7 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
     out->ctas = (int)(units < slots ? units : slots);
     out->smem = NT == 16    ? TcCfg<16>::kAlloc
                 : NT == 32  ? TcCfg<32>::kAlloc
+                : NT == 64  ? TcCfg<64>::kAlloc
                 : NT == 128 ? TcCfg<128>::kAlloc
                             : TcCfg<192>::kAlloc;
     const long long split_tiles = tiles - whole;
@@ -746,6 +745,7 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
     switch (plan.NT) {
         case 16: return launch_nt<16>(tm, prm, plan, s, pdl);
         case 32: return launch_nt<32>(tm, prm, plan, s, pdl);
+        case 64: return launch_nt<64>(tm, prm, plan, s, pdl);
         case 192: return launch_nt<192>(tm, prm, plan, s, pdl);
         default: return launch_nt<128>(tm, prm, plan, s, pdl);
     }
