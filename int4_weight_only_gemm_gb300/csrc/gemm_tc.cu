@@ -16,18 +16,20 @@
 //    weight slab (one bulk copy, 8 KB for a full tile) and the group's
 //    zero-point words; activation producer warp: the x tile (one 3-D TMA,
 //    two 64-wide 128-byte swizzled slabs); both complete one barrier;
-//  * dequant warpgroups (four for NT <= 32, two for NT = 128 / 192), taking groups
+//  * dequant warpgroups (four for NT <= 64, two for NT = 128 / 192), taking groups
 //    in turn: thread t turns column t's 16 words into 64 bfloat16 pairs
 //    (q - z) -- exact small integers: mask-and-or to 128 + q, subtract
 //    128 + z -- and writes them to tensor memory as the MMA's A operand
 //    (tcgen05.st, buffer q % SA);
-//  * MMA warp: one elected lane issues each group's 8 tcgen05.mma kind::f16
+//  * MMA warp: one elected lane waits for the group's one "ready" barrier (A
+//    buffer written, D buffer read out), issues its 8 tcgen05.mma kind::f16
 //    (A from tensor memory, B = x from shared memory) into D buffer q % NDB
 //    and commits them to the group's barrier;
 //  * rescale warpgroup(s): per group, reads D with tcgen05.ld and adds
 //    s[g][n] * D into f32 registers (the binary16 scale is applied in f32,
-//    never rounded to bfloat16); at a unit's end writes bf16 y, or split-K
-//    partials reduced in fixed order by the last CTA to arrive.
+//    never rounded to bfloat16); at a unit's end writes bf16 y (or, for fused
+//    gate/up weights, silu(gate) * up), or token-major split-K partials
+//    reduced in fixed order by the last CTA to arrive.
 //
 // For NT >= 128 a rescale thread holds 64 or 96 accumulators: its warpgroups raise
 // their register budget (setmaxnreg) with registers the dequant warpgroups and

@@ -4,7 +4,8 @@
 // Quantize the Drafter" (pith.science review, "Assumptions & free parameters":
 // packing puts weights back onto the frozen per-group grid): every 4-bit code
 // keeps its value, only its position changes.  The device layout is defined
-// in include/w4a16.h.
+// in include/w4a16.h; fused gate/up weights (guH > 0) first put their columns
+// in the interleaved order of gu_column (kernels.h).
 #include "common.cuh"
 #include "kernels.h"
 
