@@ -156,37 +156,52 @@ def run_reference(args, rank, world):
     cfg_name, seed, items = wi.CONFIGS[1]
     probs = [wi.generate_named(s, M, seed) for (s, M) in items]
     total_steps = args.steps + args.warmup
-    # per-step sample: a column window of every projection, sized so that the
-    # whole run stays near `budget` seconds of CPU work
+    # Per-step sample: a window of w columns of every projection (four windows
+    # per projection, taken in turn), w sized from a calibration of the step
+    # time t(w) = a + b w so that the whole run stays near `budget` seconds.
+    # Many short steps run single-threaded: a parallel region per call would
+    # cost more than the call itself.
     budget = 60.0
-    full_bytes = sum(gemm_bytes(p.M, p.K, p.N) for p in probs)
-    t0 = time.perf_counter()
-    oracle.gemm(probs[0].x, probs[0].qweight[:, :256].copy(), probs[0].scales[:, :256].copy(),
-                probs[0].qzeros[:, :32].copy())
-    per_col = (time.perf_counter() - t0) / 256 * (full_bytes / gemm_bytes(1, probs[0].K, probs[0].N)) / probs[0].N
-    frac = min(1.0, max(budget / max(total_steps, 1) / max(per_col * probs[0].N, 1e-9), 0.0))
-    windows = []
-    for p in probs:
-        w = max(8, int(p.N * frac) // 8 * 8)
-        w = min(w, p.N)
-        sl = []
-        for i in range(4):
-            c0 = ((p.N - w) * i // 4) // 8 * 8
-            sl.append((p.x, np.ascontiguousarray(p.qweight[:, c0:c0 + w]),
-                       np.ascontiguousarray(p.scales[:, c0:c0 + w]),
-                       np.ascontiguousarray(p.qzeros[:, c0 // 8:(c0 + w) // 8]), p.M, p.K, w))
-        windows.append(sl)
+    threads = 1 if total_steps > 200 else oracle.max_threads()
+
+    def make_windows(w):
+        windows = []
+        for p in probs:
+            ww = min(max(8, w // 8 * 8), p.N)
+            sl = []
+            for i in range(4):
+                c0 = ((p.N - ww) * i // 4) // 8 * 8
+                sl.append((p.x, np.ascontiguousarray(p.qweight[:, c0:c0 + ww]),
+                           np.ascontiguousarray(p.scales[:, c0:c0 + ww]),
+                           np.ascontiguousarray(p.qzeros[:, c0 // 8:(c0 + ww) // 8]), p.M, p.K, ww))
+            windows.append(sl)
+        return windows
+
+    def step_time(windows, reps):
+        oracle.gemm(*windows[0][0][:4], nthreads=threads)  # library load, thread start
+        t0 = time.perf_counter()
+        for i in range(reps):
+            for sl in windows:
+                oracle.gemm(*sl[i % 4][:4], nthreads=threads)
+        return (time.perf_counter() - t0) / reps
+
+    t8 = step_time(make_windows(8), 20)
+    t64 = step_time(make_windows(64), 5)
+    b = max((t64 - t8) / 56.0, 1e-9)
+    a = max(t8 - 8 * b, 0.0)
+    per_step = budget / max(total_steps, 1)
+    w = int((per_step - a) / b) if per_step > a else 8
+    windows = make_windows(w)
     step_bytes = sum(gemm_bytes(sl[0][4], sl[0][5], sl[0][6]) for sl in windows)
-    threads = oracle.max_threads()
     for i in range(args.warmup):
         for sl in windows:
-            a = sl[i % 4]
-            oracle.gemm(a[0], a[1], a[2], a[3])
+            c = sl[i % 4]
+            oracle.gemm(c[0], c[1], c[2], c[3], nthreads=threads)
     t0 = time.perf_counter()
     for i in range(args.steps):
         for sl in windows:
-            a = sl[i % 4]
-            oracle.gemm(a[0], a[1], a[2], a[3])
+            c = sl[i % 4]
+            oracle.gemm(c[0], c[1], c[2], c[3], nthreads=threads)
     dt = time.perf_counter() - t0
     value = step_bytes * args.steps / dt / 1e9
     cols = [(items[j][0], windows[j][0][6], p.N) for j, p in enumerate(probs)]
