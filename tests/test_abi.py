@@ -95,3 +95,41 @@ def test_binding_imports_without_gpu(lib):
     import int4_weight_only_gemm_gb300 as w
     assert w.load_library() is not None
     assert w.w4a16_status_str(-5).startswith("a bounded")
+
+
+def test_gate_up_validation(lib):
+    vp, ci, cu, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
+    lib.w4a16_pack_gate_up.argtypes = [vp, vp, ci, ci, vp]
+    lib.w4a16_unpack_gate_up.argtypes = [vp, vp, ci, ci, vp]
+    lib.w4a16_gemm_gate_up_silu.argtypes = [ci, cu, vp, vp, vp, vp, ci, ci, ci, ci, vp, vp, sz, vp]
+    assert lib.w4a16_pack_gate_up(None, B, 256, 64, None) == -1
+    assert lib.w4a16_pack_gate_up(A, B, 256, 0, None) == -1
+    assert lib.w4a16_pack_gate_up(A, B, 256, 32, None) == -3      # H % 64
+    assert lib.w4a16_pack_gate_up(A, B, 200, 64, None) == -3      # K % 128
+    assert lib.w4a16_pack_gate_up(A + 4, B, 256, 64, None) == -2
+    assert lib.w4a16_pack_gate_up(A, A + 16, 256, 64, None) == -1  # overlap
+    assert lib.w4a16_unpack_gate_up(A, None, 256, 64, None) == -1
+
+    def gu(x, y, M=1, H=64, K=256, group=128, flags=1):
+        return lib.w4a16_gemm_gate_up_silu(0, flags, x, B, C, D, M, H, K, group, y, None, 0, None)
+
+    assert gu(None, E) == -1
+    assert gu(A, None) == -1
+    assert gu(A, E, H=0) == -1
+    assert gu(A, E, H=96) == -3       # H % 64
+    assert gu(A, E, K=320) == -3      # K % 128
+    assert gu(A, E, group=64) == -3
+    assert gu(A, E, flags=4) == -1    # unknown flag bit
+    assert gu(A + 2, E) == -2
+    assert gu(A, E + 8) == -2
+    assert gu(A, A + 64) == -1        # y [1][64] bf16 overlapping x
+
+
+def test_requant_validation(lib):
+    vp, ci = ctypes.c_void_p, ctypes.c_int
+    lib.w4a16_requant_pack.argtypes = [vp, vp, vp, ci, ci, ci, vp, vp]
+    assert lib.w4a16_requant_pack(None, C, D, 256, 128, 128, B, None) == -1
+    assert lib.w4a16_requant_pack(A, C, D, 256, 128, 64, B, None) == -3
+    assert lib.w4a16_requant_pack(A, C, D, 256, 12, 128, B, None) == -1
+    assert lib.w4a16_requant_pack(A + 2, C, D, 256, 128, 128, B, None) == -2
+    assert lib.w4a16_requant_pack(A, C, D, 256, 128, 128, A + 16, None) == -1  # codes over w
