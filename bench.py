@@ -153,7 +153,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     import oracle
-    cfg_name, seed, items = wi.CONFIGS[1]
+    seed, items = wi.WORKLOADS["decode_m1"]
     probs = [wi.generate_named(s, M, seed) for (s, M) in items]
     total_steps = args.steps + args.warmup
     # Per-step sample: a window of w columns of every projection (four windows
@@ -362,7 +362,7 @@ def measure_e2e(w, torch, wl, steps):
 def cpu_baseline(min_seconds=8.0, one_core_seconds=3.0):
     """The oracle on the host cores: all of them (OpenMP default), then one."""
     import oracle
-    _, seed, items = wi.CONFIGS[1]
+    seed, items = wi.WORKLOADS["decode_m1"]
     probs = [wi.generate_named(s, M, seed) for (s, M) in items]
     step_bytes = sum(gemm_bytes(p.M, p.K, p.N) for p in probs)
     cores = oracle.max_threads()
@@ -544,7 +544,7 @@ def main():
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
 
-    _, seed1, items1 = wi.CONFIGS[1]
+    seed1, items1 = wi.WORKLOADS["decode_m1"]
     wl = Workload(w, torch, items1, seed1, COPIES, device)
     per_step, rot = wl.graphs()
     launches0 = w.w4a16_launch_count()
@@ -579,12 +579,13 @@ def main():
             t_ms = time_graph_steps(torch, ps, rt, COPIES, n, 50)
             fl[name] = {"us_per_step": t_ms / n * 1e3, "GB/s": wl.bytes * n / (t_ms / 1e3) / 1e9}
         extra["decode_m1_flags"] = fl
-        for cfg, unit in ((2, "GB/s"), (3, "TFLOP/s")):
-            name, seed, items = wi.CONFIGS[cfg]
-            copies = COPIES if cfg == 2 else 2
+        for name, unit in (("verify_m16", "GB/s"), ("prefill_m2048", "TFLOP/s")):
+            seed, items = wi.WORKLOADS[name]
+            small = unit == "GB/s"
+            copies = COPIES if small else 2
             wl2 = Workload(w, torch, items, seed, copies, device)
             ps, rt = wl2.graphs()
-            n = 4000 if cfg == 2 else 40
+            n = 4000 if small else 40
             t_ms = time_graph_steps(torch, ps, rt, copies, n, 10)
             if unit == "GB/s":
                 v = wl2.bytes * n / (t_ms / 1e3) / 1e9
@@ -595,7 +596,7 @@ def main():
             per2 = {}
             for i, g in enumerate(wl2.gemms):
                 ps1, rt1 = wl2.graphs(only=i)
-                n1 = 2000 if cfg == 2 else 20
+                n1 = 2000 if small else 20
                 t1 = time_graph_steps(torch, ps1, rt1, copies, n1, 5)
                 per2[g["shape"]] = {"us": t1 / n1 * 1e3,
                                     "GB/s": gemm_bytes(g["M"], g["K"], g["N"]) * n1 / (t1 / 1e3) / 1e9,

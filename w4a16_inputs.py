@@ -43,14 +43,14 @@ SHAPES = {
 SHAPE_INDEX = {"qkv": 0, "o_proj": 1, "gate_up": 2, "down": 3, "vocab": 4}
 LAYER = ("qkv", "o_proj", "gate_up", "down")
 
-# Workloads: (name, seed, list of (shape name, M)).
-CONFIGS = {
-    0: ("tiny", 0, [("tiny", 1)]),
-    1: ("decode_m1", 1, [(s, 1) for s in LAYER]),
-    2: ("verify_m16", 2, [(s, 16) for s in LAYER]),
-    3: ("prefill_m2048", 3, [(s, 2048) for s in LAYER]),
-    4: ("sweep", 4, [(s, m) for m in (1, 2, 4, 8, 16, 32, 64, 128, 8192) for s in LAYER]
-        + [("vocab", 1), ("vocab", 16)]),
+# Workloads by name: (seed, list of (shape name, M)).
+WORKLOADS = {
+    "tiny": (0, [("tiny", 1)]),
+    "decode_m1": (1, [(s, 1) for s in LAYER]),
+    "verify_m16": (2, [(s, 16) for s in LAYER]),
+    "prefill_m2048": (3, [(s, 2048) for s in LAYER]),
+    "sweep": (4, [(s, m) for m in (1, 2, 4, 8, 16, 32, 64, 128, 8192) for s in LAYER]
+              + [("vocab", 1), ("vocab", 16)]),
 }
 TINY = (256, 128)
 
