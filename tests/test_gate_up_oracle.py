@@ -85,3 +85,40 @@ def test_fused_one_hot_closed_form():
     want = g / (1.0 + np.exp(-g)) * u
     np.testing.assert_allclose(oracle.gemm_gate_up_silu(x, p.qweight, p.scales, p.qzeros, H)[0], want,
                                rtol=1e-15, atol=1e-15)
+
+
+# ---- the pins above catch plausible mistakes in the epilogue (planted here, on the CPU) ----
+
+def _pins_hold(silu_mul):
+    """The hand-worked, identity and half-order pins, applied to a candidate rendering."""
+    ok = abs(silu_mul(np.array([[np.log(3.0), 2.0]]), 1)[0, 0] - 1.5 * np.log(3.0)) < 1e-12
+    g = np.linspace(-8, 8, 33)
+    ones = np.ones_like(g)
+    s_pos = silu_mul(np.stack([g, ones], axis=1), 1)[:, 0]
+    s_neg = silu_mul(np.stack([-g, ones], axis=1), 1)[:, 0]
+    ok = ok and np.allclose(s_neg, s_pos - g, atol=1e-12)
+    ok = ok and abs(silu_mul(np.array([[2.0, 5.0]]), 1)[0, 0] - 2.0 / (1.0 + np.exp(-2.0)) * 5.0) < 1e-12
+    return bool(ok)
+
+
+def _halves(y, H):
+    y = np.asarray(y, dtype=np.float64)
+    return y[..., :H], y[..., H:]
+
+
+MUTANTS = {
+    "halves swapped": lambda y, H: (lambda g, u: u / (1.0 + np.exp(-u)) * g)(*_halves(y, H)),
+    "exp sign": lambda y, H: (lambda g, u: g / (1.0 + np.exp(g)) * u)(*_halves(y, H)),
+    "sigmoid only": lambda y, H: (lambda g, u: 1.0 / (1.0 + np.exp(-g)) * u)(*_halves(y, H)),
+    "no gate factor": lambda y, H: (lambda g, u: g * u)(*_halves(y, H)),
+    "tanh gate": lambda y, H: (lambda g, u: g * 0.5 * (1.0 + np.tanh(g)) * u)(*_halves(y, H)),
+}
+
+
+def test_pins_hold_for_the_oracle():
+    assert _pins_hold(oracle.silu_mul)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_a_planted_mistake(name):
+    assert not _pins_hold(MUTANTS[name]), f"the pins miss the mistake: {name}"
