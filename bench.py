@@ -475,6 +475,16 @@ def measure_gate_up_silu(w, torch, device, hbm, bf16_peak):
     return out
 
 
+def max_over_ranks(dist, torch, value: float, device) -> float:
+    """The largest of the ranks' values (the slowest rank's time); the value
+    itself without a process group."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_case(case, reps):
     """One seeded GEMM of the named layer shape, launched `reps` times back to
     back on the current stream (the workload of the ncu summaries)."""
@@ -552,10 +562,7 @@ def main():
         ms = time_graph_steps(torch, per_step, rot, COPIES, args.steps, args.warmup, barrier)
     clocks = clk.summary()
     launches_in_graphs = len(wl.gemms) * args.steps  # graph replays do not pass through the library
-    if dist is not None:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(dist, torch, ms, device)
     ms_step = ms / args.steps
     value = wl.bytes * args.steps * world / (ms / 1e3) / 1e9
 
