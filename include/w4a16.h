@@ -80,8 +80,11 @@ typedef enum {
  */
 typedef enum {
     W4A16_PATH_AUTO = 0,
-    W4A16_PATH_GEMV = 1,      /* CUDA-core split-K GEMV, M <= 8 */
-    W4A16_PATH_TC = 2         /* tcgen05 tensor-core GEMM, any M */
+    W4A16_PATH_GEMV = 1,      /* CUDA-core GEMV, M <= 8: the column-sliced form when the
+                                 columns fill the GPU, else the split-K form */
+    W4A16_PATH_TC = 2,        /* tcgen05 tensor-core GEMM, any M */
+    W4A16_PATH_GEMV_SPLITK = 3, /* CUDA-core GEMV, split-K form forced (M <= 8) */
+    W4A16_PATH_GEMV_CS = 4    /* CUDA-core GEMV, column-sliced form forced (M <= 8) */
 } w4a16_path;
 
 /*
@@ -251,7 +254,10 @@ int w4a16_last_device_status(w4a16_stream_t stream);
 int w4a16_selftest_wait_timeout(long long wait_ns, w4a16_stream_t stream);
 
 /* Size of the scratch array built into the library for w4a16_gemm_noalloc:
- * 4 MiB, held on every GPU that loads the library until the process exits. */
+ * 4 MiB, held on every GPU that loads the library until the process exits.
+ * The GEMV needs 64 KiB of arrival counters plus 4 KiB of f32 partial sums per
+ * CTA at most (one CTA per SM: about 0.7 MiB on a 152-SM GPU), so every
+ * M <= 8 problem fits; the size check is a guard, not a limit met in use. */
 #define W4A16_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 /*
@@ -279,7 +285,9 @@ int w4a16_gemm_noalloc(const void *x, const uint32_t *qweight_dev, const void *s
                        const uint32_t *qzeros, int M, int N, int K, int group, void *y,
                        w4a16_stream_t stream);
 
-/* Number of kernel launches the library has issued in this process. */
+/* Number of kernel launches the library has issued in this process (every
+ * entry point that launches counts its kernel; w4a16_gemm_noalloc's counter
+ * memset is not a kernel launch). */
 uint64_t w4a16_launch_count(void);
 
 #ifdef __cplusplus

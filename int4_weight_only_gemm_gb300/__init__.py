@@ -33,7 +33,7 @@ W4A16_EUNSUPPORTED = -3
 W4A16_ECUDA = -4
 W4A16_ETIMEOUT = -5
 W4A16_EWORKSPACE = -6
-PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
+PATH_AUTO, PATH_GEMV, PATH_TC, PATH_GEMV_SPLITK, PATH_GEMV_CS = 0, 1, 2, 3, 4
 FLAG_PDL, FLAG_STATIC_WEIGHTS = 1, 2
 
 _lib = None
@@ -196,9 +196,10 @@ def w4a16_gemm_gate_up_silu(x: torch.Tensor, qweight_dev: torch.Tensor, scales: 
         out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
     _check(out, "out", torch.bfloat16, (M, H))
     lib = load_library()
-    need = int(lib.w4a16_workspace_bytes_path(path, M, N, K, group))
-    if workspace is None and need:
-        workspace = _cached_workspace(need, x.device)
+    if workspace is None:
+        need = _workspace_need(path, M, N, K, group, x.device)
+        if need:
+            workspace = _cached_workspace(need, x.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib.w4a16_gemm_gate_up_silu(path, FLAG_PDL if flags is None else flags, x.data_ptr(),
@@ -231,6 +232,19 @@ def w4a16_set_workspace(workspace: torch.Tensor | None) -> None:
 
 
 _ws_cache: dict[int, torch.Tensor] = {}
+_need_cache: dict[tuple, int] = {}
+
+
+def _workspace_need(path: int, M: int, N: int, K: int, group: int, device: torch.device) -> int:
+    """Workspace bytes a problem needs, asked of the library once per problem
+    and device (the answer depends only on these)."""
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    key = (path, M, N, K, group, idx)
+    need = _need_cache.get(key)
+    if need is None:
+        need = int(load_library().w4a16_workspace_bytes_path(path, M, N, K, group))
+        _need_cache[key] = need
+    return need
 
 
 def _cached_workspace(nbytes: int, device: torch.device) -> torch.Tensor:
@@ -262,9 +276,10 @@ def w4a16_gemm(x: torch.Tensor, qweight_dev: torch.Tensor, scales: torch.Tensor,
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _check(out, "out", torch.bfloat16, (M, N))
     lib = load_library()
-    need = int(lib.w4a16_workspace_bytes_path(path, M, N, K, group))
-    if workspace is None and need:
-        workspace = _cached_workspace(need, x.device)
+    if workspace is None:
+        need = _workspace_need(path, M, N, K, group, x.device)
+        if need:
+            workspace = _cached_workspace(need, x.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     if flags is None:

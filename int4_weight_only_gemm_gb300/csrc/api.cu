@@ -51,24 +51,6 @@ int check_kn(int N, int K) {
     return W4A16_OK;
 }
 
-// ny: columns of y (N for the plain product, N / 2 for the fused gate/up one)
-int check_gemm(const void* x, const uint32_t* qd, const void* scales, const uint32_t* qzeros, int M, int N, int K,
-               int group, void* y, int ny) {
-    if (!x || !qd || !scales || !qzeros || !y) return W4A16_EINVAL;
-    if (M < 1) return W4A16_EINVAL;
-    if (group != 128) return W4A16_EUNSUPPORTED;
-    int st = check_kn(N, K);
-    if (st != W4A16_OK) return st;
-    if (!aligned16(x) || !aligned16(qd) || !aligned16(y) || !aligned16(scales) || !aligned16(qzeros))
-        return W4A16_EALIGN;
-    const size_t ybytes = (size_t)M * ny * 2;
-    const int G = K / group;
-    if (overlaps(y, ybytes, x, (size_t)M * K * 2) || overlaps(y, ybytes, qd, (size_t)K / 2 * N) ||
-        overlaps(y, ybytes, scales, (size_t)G * N * 2) || overlaps(y, ybytes, qzeros, (size_t)G * N / 2))
-        return W4A16_EINVAL;
-    return W4A16_OK;
-}
-
 // Fused gate/up weights: H = columns of each half, a multiple of 64 so that
 // every 128-column device tile holds 64 gate and 64 up columns.
 int check_gate_up(int H, int K) {
@@ -90,23 +72,45 @@ int repack_gate_up(bool pack, const uint32_t* src, uint32_t* dst, int K, int H, 
     return W4A16_OK;
 }
 
+// The column-sliced GEMV gives every CTA whole columns: no split-K hand-off,
+// which dominates small matrices, but its register-ring stream is slower than
+// the split-K form's bulk copies once a CTA has much to read (measured on the
+// decoder's shapes at M = 1: 4.4 / 4.6 us against 5.4 / 5.6 us for qkv and
+// o_proj, 36 KB a CTA; 14.4 / 9.8 us against 9.0 / 7.5 us for gate_up and
+// down, 170 and 85 KB a CTA).  It is the GEMV's form when every SM gets a
+// slice of at most 64 KB of packed weights.
+constexpr long long kCsMaxCtaBytes = 64 << 10;
+bool gemv_uses_cs(int M, int N, int K, int sms, int guH, GemvCsPlan* cp) {
+    return gemv_cs_plan(M, N, K, sms, guH, cp) && cp->ctas >= sms &&
+           (long long)K * N / 2 <= kCsMaxCtaBytes * cp->ctas;
+}
+
 // Kernel choice per M, from measured times on GB300 (layer shapes of a ~4B
 // decoder, M = 1..8): the GEMV's arithmetic grows with M while the
 // tensor-core kernel's time is flat in M, and they cross between M = 2 and
 // M = 4, later for smaller weight matrices.  GEMV when M <= 2, or M <= 4 with
-// at most 16M weights, and its activation copy fits in shared memory.
+// at most 16M weights, and it fits in shared memory; the tensor-core GEMM
+// otherwise.
 int choose_path(int M, int N, int K, int sms) {
     GemvPlan gp;
+    GemvCsPlan cp;
     const bool small = (long long)K * N <= (16ll << 20);
-    if ((M <= 2 || (M <= 4 && small)) && gemv_plan(M, N, K, sms, &gp)) return W4A16_PATH_GEMV;
+    if ((M <= 2 || (M <= 4 && small)) && (gemv_cs_plan(M, N, K, sms, 0, &cp) || gemv_plan(M, N, K, sms, &gp)))
+        return W4A16_PATH_GEMV;
     return W4A16_PATH_TC;
 }
 
 size_t ws_for_path(int path, int M, int N, int K, int sms) {
+    GemvPlan gp;
+    GemvCsPlan cp;
+    if (path == W4A16_PATH_GEMV_CS) return 0;
     if (path == W4A16_PATH_GEMV) {
-        GemvPlan gp;
-        return gemv_plan(M, N, K, sms, &gp) ? gp.ws_bytes : 0;
+        // no workspace when both the plain and the fused gate/up product of
+        // this N take the column-sliced form
+        if (gemv_uses_cs(M, N, K, sms, 0, &cp) && gemv_uses_cs(M, N, K, sms, N / 2, &cp)) return 0;
+        path = W4A16_PATH_GEMV_SPLITK;
     }
+    if (path == W4A16_PATH_GEMV_SPLITK) return gemv_plan(M, N, K, sms, &gp) ? gp.ws_bytes : 0;
     TcPlan tp;
     return tc_plan(M, N, K, sms, &tp) ? tp.ws_bytes : 0;
 }
@@ -129,7 +133,13 @@ int run_gemm(int path, unsigned flags, const void* x, const uint32_t* qd, const 
     if (sms <= 0) return W4A16_ECUDA;
     if (path == W4A16_PATH_AUTO) path = choose_path(M, N, K, sms);
     cudaError_t e;
-    if (path == W4A16_PATH_GEMV) {
+    GemvCsPlan cp;
+    if (path == W4A16_PATH_GEMV) path = gemv_uses_cs(M, N, K, sms, guH, &cp) ? W4A16_PATH_GEMV_CS : W4A16_PATH_GEMV_SPLITK;
+    if (path == W4A16_PATH_GEMV_CS) {
+        if (!gemv_cs_plan(M, N, K, sms, guH, &cp)) return W4A16_EUNSUPPORTED;
+        e = launch_gemv_cs(static_cast<const uint16_t*>(x), qd, static_cast<const uint16_t*>(scales), qzeros,
+                           static_cast<uint16_t*>(y), M, N, K, cp, stream, flags, guH);
+    } else if (path == W4A16_PATH_GEMV_SPLITK) {
         GemvPlan gp;
         if (!gemv_plan(M, N, K, sms, &gp)) return W4A16_EUNSUPPORTED;
         if (gp.ws_bytes && (!ws || ws_bytes < gp.ws_bytes || !aligned16(ws))) return W4A16_EWORKSPACE;
@@ -150,6 +160,28 @@ int run_gemm(int path, unsigned flags, const void* x, const uint32_t* qd, const 
 }
 
 }  // namespace
+
+// Argument rules of every GEMM entry point (also used by w4a16_gemm_noalloc).
+// ny: columns of y (N for the plain product, N / 2 for the fused gate/up one)
+int check_gemm(const void* x, const uint32_t* qd, const void* scales, const uint32_t* qzeros, int M, int N, int K,
+               int group, void* y, int ny) {
+    if (!x || !qd || !scales || !qzeros || !y) return W4A16_EINVAL;
+    if (M < 1) return W4A16_EINVAL;
+    if (group != 128) return W4A16_EUNSUPPORTED;
+    int st = check_kn(N, K);
+    if (st != W4A16_OK) return st;
+    if (!aligned16(x) || !aligned16(qd) || !aligned16(y) || !aligned16(scales) || !aligned16(qzeros))
+        return W4A16_EALIGN;
+    const size_t ybytes = (size_t)M * ny * 2;
+    const int G = K / group;
+    if (overlaps(y, ybytes, x, (size_t)M * K * 2) || overlaps(y, ybytes, qd, (size_t)K / 2 * N) ||
+        overlaps(y, ybytes, scales, (size_t)G * N * 2) || overlaps(y, ybytes, qzeros, (size_t)G * N / 2))
+        return W4A16_EINVAL;
+    return W4A16_OK;
+}
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 }  // namespace w4a16
 
 using namespace w4a16;
@@ -239,7 +271,7 @@ size_t w4a16_workspace_bytes_max(int max_M, int N, int K, int group) {
     for (int m = 1; m <= max_M; ++m) {
         // the plan only changes at token-tile boundaries; probe each M up to 256, then tile edges
         if (m > 256 && (m % 128) != 0 && m != max_M) continue;
-        for (int path = W4A16_PATH_GEMV; path <= W4A16_PATH_TC; ++path) {
+        for (int path = W4A16_PATH_GEMV; path <= W4A16_PATH_GEMV_CS; ++path) {
             size_t b = w4a16_workspace_bytes_path(path, m, N, K, group);
             if (b > best) best = b;
         }

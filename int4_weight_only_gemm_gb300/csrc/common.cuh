@@ -209,6 +209,14 @@ W4A16_DEVICE void tma_load_2d(void* smem_dst, const void* tmap, int x, int y, ui
 W4A16_DEVICE void cp_async_4(void* smem_dst, const void* gsrc) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
 }
+// 8- and 16-byte asynchronous copies global -> shared (both addresses aligned
+// to the size); the 16-byte form bypasses L1.
+W4A16_DEVICE void cp_async_8(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+W4A16_DEVICE void cp_async_16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
 // Close the group of this thread's cp.async copies issued since the last commit.
 W4A16_DEVICE void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's committed cp.async groups are pending.

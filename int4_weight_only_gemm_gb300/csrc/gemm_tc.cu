@@ -76,19 +76,27 @@ struct TcParams {
     int guH;         // > 0: fused gate/up weights (N = 2 guH); y[M][guH] = silu(gate) * up
 };
 
-// Configuration per token-tile width NT (one CTA per SM).
-template <int NT>
+// Configuration per token-tile width NT.  HALF: a configuration that takes at
+// most half of an SM (two dequant warpgroups, a shorter ring, 256 tensor-memory
+// columns, at most 64 registers a thread), so that two CTAs run on every SM:
+// each has its own MMA-issuing thread, and one thread issues tcgen05.mma at
+// only about half the rate an SM's tensor core sustains for small N
+// (measured: ~49 ns per M = 128, K = 16 instruction with a commit and wait
+// per group, whether one or two CTAs share the SM).
+template <int NT, bool HALF = false>
 struct TcCfg {
+    static_assert(!HALF || NT <= 32, "the half-SM configuration is for small token tiles");
     static constexpr int R = NT >= 64 ? 2 : 1;           // rescale warpgroups, each owning NT/R columns
-    static constexpr int SS = NT <= 16 ? 12 : NT <= 32 ? 10 : NT <= 64 ? 8 : NT <= 128 ? 4 : 3;  // shared-memory ring stages
-    static constexpr int SA = NT <= 64 ? 4 : NT <= 128 ? 3 : 2;  // A buffers in tensor memory (q % SA)
-    static constexpr int NDB = ((512 - SA * 64) / NT) < 8 ? ((512 - SA * 64) / NT) : 8;  // D accumulator ring
+    static constexpr int SS = HALF ? (NT <= 16 ? 8 : 6) : NT <= 16 ? 12 : NT <= 32 ? 10 : NT <= 64 ? 8 : NT <= 128 ? 4 : 3;  // shared-memory ring stages
+    static constexpr int SA = HALF ? 2 : NT <= 64 ? 4 : NT <= 128 ? 3 : 2;  // A buffers in tensor memory (q % SA)
+    static constexpr int kTmemBudget = HALF ? 256 : 512;
+    static constexpr int NDB = ((kTmemBudget - SA * 64) / NT) < 8 ? ((kTmemBudget - SA * 64) / NT) : 8;  // D accumulator ring
     static constexpr int kDone = 16;                     // ring of "MMAs of group q done" barriers
     // ring of "group q may be issued" barriers: its A buffer written and its D
     // buffer read out (arrivals for q follow the completion of q - SA and of
     // q - NDB, so max(SA, NDB) slots keep the phases apart)
     static constexpr int kReady = SA > NDB ? SA : NDB;
-    static constexpr int kDeqWG = NT <= 64 ? 4 : 2;      // dequant warpgroups, taking groups q % kDeqWG
+    static constexpr int kDeqWG = HALF ? 2 : NT <= 64 ? 4 : 2;  // dequant warpgroups, taking groups q % kDeqWG
     static constexpr int kDeqWarps = 4 * kDeqWG;
     static constexpr int kResWarp0 = kDeqWarps;          // rescale warpgroups follow
     static constexpr int kMmaWarp = kDeqWarps + 4 * R;   // then the MMA warp (the only tcgen05.mma issuer)
@@ -101,6 +109,7 @@ struct TcCfg {
     static constexpr bool kRegSplit = NT >= 128;
     static constexpr int kWarps = kRegSplit ? (kXWarp + 4) / 4 * 4 : kXWarp + 1;
     static constexpr int kThreads = 32 * kWarps;
+    static constexpr int kMinBlocks = HALF ? 2 : 1;      // CTAs per SM the launch bounds ask for
     static constexpr int kRegDeq = 64, kRegRes = 144, kRegMisc = 64;  // per thread, after the split
     static constexpr int kRegPool =
         32 * (kDeqWarps * kRegDeq + 4 * R * kRegRes + (kWarps - kDeqWarps - 4 * R) * kRegMisc);
@@ -124,6 +133,8 @@ struct TcCfg {
     static constexpr int kTmemUsed = SA * 64 + NDB * NT;
     static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
     static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+    static_assert(!HALF || (kAlloc <= 113 * 1024 && kTmemCols <= 256 && kThreads * 64 * 2 <= 65536),
+                  "two CTAs per SM");
     static_assert(kTmemUsed <= 512, "tensor memory budget");
 };
 
@@ -170,10 +181,10 @@ W4A16_DEVICE void tmem_st_x32(uint32_t taddr, const uint32_t* v) {
         : "memory");
 }
 
-template <int NT>
-__global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
+template <int NT, bool HALF>
+__global__ void __launch_bounds__(TcCfg<NT, HALF>::kThreads, TcCfg<NT, HALF>::kMinBlocks)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcParams p) {
-    using C = TcCfg<NT>;
+    using C = TcCfg<NT, HALF>;
     constexpr int SS = C::SS;
     constexpr int SA = C::SA;
     constexpr int R = C::R;
@@ -608,13 +619,19 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
 // beside two A buffers in the 512 tensor-memory columns.  Up to 256 tokens
 // the shorter per-group chain of 128-token tiles measured faster.
 static int tc_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 256 ? 128 : 192; }
+// Token tiles of up to kTcHalfMaxNT tokens run the half-SM configuration,
+// two CTAs per SM.  Off: measured at M = 16 and 32 on the decoder's shapes it
+// was slower (verify step 40.7 -> 46.9 us), the two CTAs sharing the SM's copy
+// engine, which the three copies per group already keep busy.
+constexpr int kTcHalfMaxNT = 0;
 
 bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
     const Layout L(K, N);
     const int G = K / 128;
     const int NT = tc_nt(M);
     const int MT = (M + NT - 1) / NT;
-    const long long slots = sms;  // one CTA per SM
+    const bool half = NT <= kTcHalfMaxNT;
+    const long long slots = half ? 2ll * sms : sms;  // CTAs resident at once
     const long long tiles = (long long)L.NB * MT;
     const int max_split = G / 2 > 0 ? G / 2 : 1;  // at least 2 groups a piece
     long long whole = tiles;
@@ -656,8 +673,9 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
     out->splits = splits;
     out->units = (int)units;
     out->ctas = (int)(units < slots ? units : slots);
-    out->smem = NT == 16    ? TcCfg<16>::kAlloc
-                : NT == 32  ? TcCfg<32>::kAlloc
+    out->half = half;
+    out->smem = NT == 16    ? (half ? TcCfg<16, true>::kAlloc : TcCfg<16>::kAlloc)
+                : NT == 32  ? (half ? TcCfg<32, true>::kAlloc : TcCfg<32>::kAlloc)
                 : NT == 64  ? TcCfg<64>::kAlloc
                 : NT == 128 ? TcCfg<128>::kAlloc
                             : TcCfg<192>::kAlloc;
@@ -683,29 +701,30 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-template <int NT>
+template <int NT, bool HALF = false>
 static cudaError_t launch_nt(const CUtensorMap& tm, const TcParams& prm, const TcPlan& plan, cudaStream_t s,
                              bool pdl) {
-    auto kern = tc_gemm_kernel<NT>;
+    using C = TcCfg<NT, HALF>;
+    auto kern = tc_gemm_kernel<NT, HALF>;
     static int set_for[64];  // shared memory limit raised once per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!set_for[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<NT>::kAlloc);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kAlloc);
         if (e != cudaSuccess) return e;
-        if (TcCfg<NT>::kRegSplit) {
+        if (C::kRegSplit) {
             // the warpgroups' register budgets must fit in what the CTA is
             // launched with, or the increase would wait forever: never launch then
             cudaFuncAttributes fa;
             e = cudaFuncGetAttributes(&fa, kern);
             if (e != cudaSuccess) return e;
-            if ((long long)fa.numRegs * TcCfg<NT>::kThreads < TcCfg<NT>::kRegPool) return cudaErrorInvalidConfiguration;
+            if ((long long)fa.numRegs * C::kThreads < C::kRegPool) return cudaErrorInvalidConfiguration;
         }
         set_for[dev] = 1;
     }
-    return launch_kernel(kern, dim3(plan.ctas), dim3(TcCfg<NT>::kThreads), plan.smem, s, pdl, tm, prm);
+    return launch_kernel(kern, dim3(plan.ctas), dim3(C::kThreads), plan.smem, s, pdl, tm, prm);
 }
 
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
@@ -745,8 +764,8 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     prm.guH = guH;
     switch (plan.NT) {
-        case 16: return launch_nt<16>(tm, prm, plan, s, pdl);
-        case 32: return launch_nt<32>(tm, prm, plan, s, pdl);
+        case 16: return plan.half ? launch_nt<16, true>(tm, prm, plan, s, pdl) : launch_nt<16>(tm, prm, plan, s, pdl);
+        case 32: return plan.half ? launch_nt<32, true>(tm, prm, plan, s, pdl) : launch_nt<32>(tm, prm, plan, s, pdl);
         case 64: return launch_nt<64>(tm, prm, plan, s, pdl);
         case 192: return launch_nt<192>(tm, prm, plan, s, pdl);
         default: return launch_nt<128>(tm, prm, plan, s, pdl);

@@ -1,0 +1,330 @@
+// Column-sliced GEMV for M = 1..8 on CUDA cores (sm_103a).
+//
+// y[m][n] = sum_k x[m][k] (q[k][n] - z[g][n]) s[g][n], g = k / 128: the INT4
+// linear layer run at every decode step by the quantized target and drafter
+// of "Quantize the Target, Quantize the Drafter" (pith.science review,
+// referee report summary; group size 128 from "Assumptions & free
+// parameters").
+//
+// Work split: CTA b owns a contiguous slice of columns [c0, c1) over all of K
+// (slices are whole units of 4 columns, or 16 for fused gate/up weights so
+// that a gate column and its up column stay together), so no CTA ever hands
+// a partial sum to another and no workspace is needed.  Inside the CTA,
+// thread t takes column j = t % C of the slice and the range s = t / C of
+// the K split (S = 512 / C ranges), or, for slices wider than half the
+// block, whole columns j = t, t + 512, ...
+//
+// Data movement: the unit of work is an item, one column's 32 rows of K: 16
+// bytes of the device layout (word j of chunk c holds rows 8(4c + j)..+7).
+// A column's items lie a constant W * 16 bytes apart (W = width of its
+// 128-column tile), and the lanes of a warp read adjacent columns, so each
+// load instruction of a warp fetches contiguous runs.  Each thread keeps D
+// items in flight in a register ring (16-byte global loads, no L1
+// allocation): no shared-memory staging of weights at all.
+//
+// Arithmetic: per item and token, dot = sum over the 32 rows of (128 + q) x
+// with the bfloat16 value 128 + q made by one mask-and-or per pair of rows
+// (exact) and bf16 x bf16 -> f32 fused multiply-adds; the zero point and
+// scale then apply once per item in f32: acc += s (dot - (128 + z) xs), xs =
+// the sum of the item's 32 activations (computed once per CTA).  The scale
+// is used at its full binary16 precision.  The K ranges of a column are
+// added through shared memory in range order: the result does not depend on
+// timing.
+//
+// Footprint: at M <= 2 a CTA uses at most 64 registers a thread and about
+// 30 KB of shared memory for the decoder's shapes, so two CTAs fit on an SM:
+// the next programmatic-dependent GEMM of a chain becomes resident while this
+// one runs, and with static weights starts its loads before the grid
+// dependency resolves.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace w4a16 {
+
+struct CsParams {
+    const uint16_t* x;
+    const uint32_t* qd;
+    const uint16_t* scales;
+    const uint32_t* qzeros;
+    uint16_t* y;
+    int M, N, K, R, KB;  // R = K / 32 items per column
+    int U, unit;         // column units and their width (4, or 16 for fused gate/up)
+    int prefetch;        // weights, scales and zeros may be read before the preceding grid completes
+    int guH;             // > 0: fused gate/up weights (N = 2 guH); y[M][guH] = silu(gate) * up
+};
+
+constexpr int kCsThreads = 512;
+
+// Shared-memory layout (bytes from the dynamic base), identical on both
+// sides; every region starts on a 16-byte boundary.
+struct CsSmem {
+    size_t xs, xsum, sc, zr, red, total;
+    static __host__ __device__ size_t up16(size_t v) { return (v + 15) & ~(size_t)15; }
+    // MT: token rows held (M rounded up), C: slice width.  Every region grows
+    // with C, so the widest slice of a launch sizes it for all its CTAs.
+    __host__ __device__ CsSmem(int MT, int K, int C) {
+        const int R = K / 32, G = K / 128;
+        xs = 0;                                          // [MT][K] bf16 activations
+        xsum = up16(xs + (size_t)MT * K * 2);            // [MT][R] f32 item sums of x
+        sc = up16(xsum + (size_t)MT * R * 4);            // [G][C] fp16 scales of the slice
+        zr = up16(sc + (size_t)G * C * 2);               // [G][C/4] zero words, one per run of 4 columns
+        red = up16(zr + (size_t)G * C);                  // [S][C][MT] f32 partial sums (S C <= max(512, C))
+        total = up16(red + (size_t)(C > kCsThreads ? C : kCsThreads) * MT * 4);
+    }
+};
+
+__host__ __device__ inline int cs_ranges(int C, int R) {
+    int S = C >= kCsThreads / 2 ? 1 : kCsThreads / C;
+    return S < R ? S : R;
+}
+
+// 16-byte load that bypasses L1 (weights are read once).
+W4A16_DEVICE uint4 ldg_stream(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+template <int MT, int D>
+__global__ void __launch_bounds__(kCsThreads, MT <= 2 ? 2 : 1) gemv_cs_kernel(const CsParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int t = threadIdx.x;
+    const int b = blockIdx.x;
+    const int P = (int)gridDim.x;
+    const int c0 = p.unit * (int)((long long)b * p.U / P);
+    const int c1 = p.unit * (int)((long long)(b + 1) * p.U / P);
+    const int C = c1 - c0;
+    const int R = p.R, G = p.KB;
+    const int S = cs_ranges(C, R);
+    const CsSmem lay(MT, p.K, C);
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem + lay.xs);
+    float* xsum = reinterpret_cast<float*>(smem + lay.xsum);
+    uint16_t* ssc = reinterpret_cast<uint16_t*>(smem + lay.sc);
+    uint32_t* szw = reinterpret_cast<uint32_t*>(smem + lay.zr);
+    float* red = reinterpret_cast<float*>(smem + lay.red);
+
+    // the next grid in the stream may start as soon as every CTA of this one runs
+    pdl_launch_dependents();
+
+    // this thread's work: column j (then j + 512, ... when S == 1) over items [r0, r1)
+    const bool active = t < S * C || S == 1;
+    const int j0 = S == 1 ? t : t % C;
+    const int s = S == 1 ? 0 : t / C;
+    const int r0 = (int)((long long)s * R / S), r1 = (int)((long long)(s + 1) * R / S);
+    const int nr = r1 - r0;
+    const int npass = S == 1 ? (j0 < C ? (C - j0 + kCsThreads - 1) / kCsThreads : 0) : (active ? 1 : 0);
+    const int nitems = npass * nr;
+    const uint4* qd4 = reinterpret_cast<const uint4*>(p.qd);
+
+    // item address: column n, item r -> uint4 index 512 KB nb + W r + (n % 128);
+    // a column's items are W uint4 apart
+    const uint4* cptr = nullptr;
+    size_t cstride = 0;
+    uint4 ring[D];
+    // the first D items of pass `pass` (column j0 + 512 pass) into the ring
+    auto start_column = [&](int pass) {
+        const int n = c0 + j0 + pass * kCsThreads;
+        const int nb = n >> 7;
+        cstride = (size_t)(p.N - 128 * nb < 128 ? p.N - 128 * nb : 128);
+        cptr = qd4 + (size_t)512 * p.KB * nb + cstride * r0 + (n & 127);
+#pragma unroll
+        for (int i = 0; i < D; ++i)
+            if (i < nr) ring[i] = ldg_stream(cptr + i * cstride);
+    };
+    // The slice's scales ([G][C] fp16, device-column order) and, per run of
+    // four columns, the zero word holding their zero points ([G][C/4]), as
+    // asynchronous copies: every copy of the CTA is in flight at once.  Four
+    // adjacent device columns are four adjacent canonical columns in both
+    // layouts, and a column's zero nibble sits at bit 4 (n % 8) of its word.
+    auto stage_scales_zeros = [&]() {
+        const int C4 = C >> 2;
+        for (int i = t; i < G * C4; i += kCsThreads) {
+            const int g = i / C4, jj = 4 * (i - g * C4);
+            const int n = c0 + jj;
+            const int cn = p.guH ? gu_column(n, p.guH) : n;
+            cp_async_8(ssc + (size_t)g * C + jj, p.scales + (size_t)g * p.N + cn);
+            cp_async_4(szw + i, p.qzeros + (size_t)g * (p.N / 8) + (cn >> 3));
+        }
+    };
+
+    if (p.prefetch) {
+        if (npass > 0) start_column(0);
+        stage_scales_zeros();
+    }
+    pdl_wait();  // x, and y below, only after the preceding grid
+    if (!p.prefetch) {
+        if (npass > 0) start_column(0);
+        stage_scales_zeros();
+    }
+    {
+        // activations: rows m < M copied (asynchronously), rows M..MT-1 zero
+        const int n16 = MT * p.K / 8;
+        const int v16 = p.M * p.K / 8;
+        const uint4* xg = reinterpret_cast<const uint4*>(p.x);
+        uint4* xv = reinterpret_cast<uint4*>(xs);
+        for (int i = t; i < n16; i += kCsThreads) {
+            if (i < v16) cp_async_16(xv + i, xg + i);
+            else xv[i] = make_uint4(0, 0, 0, 0);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+    }
+    __syncthreads();
+    // per-item activation sums, one (token, item) per thread
+    for (int i = t; i < MT * R; i += kCsThreads) {
+        const uint4* xr = reinterpret_cast<const uint4*>(xs) + (size_t)i * 4;
+        float a = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = xr[q];
+            a += (bf16lo(v.x) + bf16hi(v.x)) + (bf16lo(v.y) + bf16hi(v.y)) + (bf16lo(v.z) + bf16hi(v.z)) +
+                 (bf16lo(v.w) + bf16hi(v.w));
+        }
+        xsum[i] = a;
+    }
+    __syncthreads();
+
+    const uint32_t xs_a = smem_u32(xs);
+    const uint32_t xrow = (uint32_t)p.K * 2;  // bytes between token rows of xs
+    for (int pass = 0; pass < npass; ++pass) {
+        if (pass > 0) start_column(pass);
+        const int jj = j0 + pass * kCsThreads;
+        const uint32_t zsh = 4u * (uint32_t)((c0 + jj) & 7);  // this column's nibble in its zero word
+        float acc[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+        // D items per round, so the ring is indexed with constants
+        for (int base = 0; base < nr; base += D) {
+#pragma unroll
+            for (int u = 0; u < D; ++u) {
+                const int i = base + u;
+                if (i < nr) {
+                    const uint32_t wv[4] = {ring[u].x, ring[u].y, ring[u].z, ring[u].w};
+                    if (i + D < nr) ring[u] = ldg_stream(cptr + (size_t)(i + D) * cstride);
+                    const int r = r0 + i;
+                    const int g = r >> 2;
+                    const float sc = f16_bits_to_f32(ssc[g * C + jj]);
+                    const float zoff = 128.f + (float)((szw[g * (C >> 2) + (jj >> 2)] >> zsh) & 0xFu);
+                    float d[MT][2];
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) d[m][0] = d[m][1] = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {  // word q: rows 8q .. 8q + 7 of the item
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            const uint4 xq = lds_v4(xs_a + (uint32_t)m * xrow + (uint32_t)r * 64 + (uint32_t)q * 16);
+                            const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
+                            float a = d[m][q & 1];
+#pragma unroll
+                            for (int pp = 0; pp < 4; ++pp) {
+                                const uint32_t wp = magic_pair(wv[q], pp);
+                                a = fma_lo(wp, xp[pp], a);
+                                a = fma_hi(wp, xp[pp], a);
+                            }
+                            d[m][q & 1] = a;
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+                        acc[m] = fmaf(sc, fmaf(-zoff, xsum[m * R + r], d[m][0] + d[m][1]), acc[m]);
+                }
+            }
+        }
+        // this column's sums over this thread's K range
+#pragma unroll
+        for (int m = 0; m < MT; ++m) red[((size_t)s * C + jj) * MT + m] = acc[m];
+    }
+    __syncthreads();
+    // the K ranges of each column added in range order; fused weights: the
+    // gate column (device column d, d % 16 < 8) meets its up column d + 8
+    for (int i = t; i < C * MT; i += kCsThreads) {
+        const int jj = i / MT, m = i - jj * MT;
+        if (m >= p.M) continue;
+        const int n = c0 + jj;
+        if (p.guH) {
+            if (n & 8) continue;  // up columns are read by their gate column
+            float g = 0.f, u = 0.f;
+            for (int r = 0; r < S; ++r) {
+                g += red[((size_t)r * C + jj) * MT + m];
+                u += red[((size_t)r * C + jj + 8) * MT + m];
+            }
+            p.y[(size_t)m * p.guH + gu_column(n, p.guH)] = f32_to_bf16_rn(silu_mul(g, u));
+        } else {
+            float v = 0.f;
+            for (int r = 0; r < S; ++r) v += red[((size_t)r * C + jj) * MT + m];
+            p.y[(size_t)m * p.N + n] = f32_to_bf16_rn(v);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+static int cs_mtile(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+constexpr int kCsMaxSmem = 226 * 1024;
+
+bool gemv_cs_plan(int M, int N, int K, int sms, int guH, GemvCsPlan* out) {
+    if (M < 1 || M > 8 || sms < 1 || K < 128 || K % 128 || N % 8) return false;
+    const int unit = guH ? 16 : 4;
+    if (N % unit) return false;
+    const long long U = N / unit;
+    const int P = (int)(U < sms ? U : sms);
+    const int MT = cs_mtile(M);
+    // the widest slice decides the shared memory
+    const int C = (int)(unit * ((U + P - 1) / P));
+    const CsSmem lay(MT, K, C);
+    if (lay.total > (size_t)kCsMaxSmem) return false;
+    out->ctas = P;
+    out->U = (int)U;
+    out->unit = unit;
+    out->smem = lay.total;
+    return true;
+}
+
+template <int MT, int D>
+static cudaError_t launch_cs(const CsParams& prm, const GemvCsPlan& plan, cudaStream_t s, bool pdl) {
+    auto kern = gemv_cs_kernel<MT, D>;
+    static int set_for[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!set_for[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCsMaxSmem);
+        if (e != cudaSuccess) return e;
+        set_for[dev] = 1;
+    }
+    return launch_kernel(kern, dim3(plan.ctas), dim3(kCsThreads), plan.smem, s, pdl, prm);
+}
+
+cudaError_t launch_gemv_cs(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
+                           uint16_t* y, int M, int N, int K, const GemvCsPlan& plan, cudaStream_t s, unsigned flags,
+                           int guH) {
+    CsParams prm;
+    prm.x = x;
+    prm.qd = qd;
+    prm.scales = scales;
+    prm.qzeros = qzeros;
+    prm.y = y;
+    prm.M = M;
+    prm.N = N;
+    prm.K = K;
+    prm.R = K / 32;
+    prm.KB = K / 128;
+    prm.U = plan.U;
+    prm.unit = plan.unit;
+    const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
+    prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
+    prm.guH = guH;
+    switch (cs_mtile(M)) {
+        case 1: return launch_cs<1, 8>(prm, plan, s, pdl);
+        case 2: return launch_cs<2, 4>(prm, plan, s, pdl);
+        case 4: return launch_cs<4, 4>(prm, plan, s, pdl);
+        default: return launch_cs<8, 4>(prm, plan, s, pdl);
+    }
+}
+
+}  // namespace w4a16

@@ -24,6 +24,13 @@ __host__ __device__ inline int gu_column(int n, int H) {
 // e^-g = inf for g < -88 gives 0)
 __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g * u, 1.f + __expf(-g)); }
 
+// Argument checks of the GEMM entry points (api.cu): W4A16_OK, or the status
+// to return without launching.  ny = columns of y (N, or H for fused gate/up).
+int check_gemm(const void* x, const uint32_t* qd, const void* scales, const uint32_t* qzeros, int M, int N, int K,
+               int group, void* y, int ny);
+// Counts one kernel launch in w4a16_launch_count (api.cu).
+void note_launch();
+
 // guH = 0: plain layout; guH = H: fused gate/up weights with N = 2H columns
 cudaError_t launch_pack(const uint32_t* q, uint32_t* qd, int K, int N, int guH, cudaStream_t s);
 cudaError_t launch_unpack(const uint32_t* qd, uint32_t* q, int K, int N, int guH, cudaStream_t s);
@@ -45,12 +52,24 @@ cudaError_t launch_gemv(const uint16_t* x, const uint32_t* qd, const uint16_t* s
                         unsigned flags, int guH);
 int gemv_read_status();
 
+// Column-sliced CUDA-core GEMV (M <= 8): every CTA owns whole columns, no workspace
+struct GemvCsPlan {
+    int ctas;        // one per SM (fewer when the columns are fewer)
+    int U, unit;     // column units and their width
+    size_t smem;
+};
+bool gemv_cs_plan(int M, int N, int K, int sms, int guH, GemvCsPlan* out);
+cudaError_t launch_gemv_cs(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
+                           uint16_t* y, int M, int N, int K, const GemvCsPlan& plan, cudaStream_t s, unsigned flags,
+                           int guH);
+
 // tcgen05 tensor-core GEMM (any M)
 struct TcPlan {
     int NT, MT, NB;          // tokens per tile, token tiles, column tiles
     int whole, splits;       // tiles [0, whole) whole, the rest in `splits` K pieces each
     int units;               // whole + (NB * MT - whole) * splits
     int ctas;                // persistent CTAs
+    bool half;               // the half-SM configuration, two CTAs per SM
     size_t smem, ws_bytes;
 };
 bool tc_plan(int M, int N, int K, int sms, TcPlan* out);

@@ -5,9 +5,10 @@ the decode set (M=1) and verify set (M=16) over the four projection shapes of
 a ~4B decoder layer, prefill (M=2048), the M sweep up to 8192 and the
 vocabulary-shaped GEMM ("Quantize the Target, Quantize the Drafter":
 pith.science review -- INT4 target and drafter, group size 128, DFlash block
-size 16).  Small problems are compared in full; full-size ones on sampled
-outputs computed one by one by the oracle.  Both kernels (GEMV and tensor
-core) are checked at every M either can run.
+size 16).  Every problem is compared in full, except M=8192, where at least
+256 whole rows are (every row of the first and last token tiles and one row
+of every other tile).  Both kernels (GEMV and tensor core) are checked at
+every M either can run.
 """
 import os
 
@@ -22,7 +23,8 @@ from tests.gpu_helpers import Device, bf16_bits, bf16_to_f64, check_close, check
 pytestmark = pytest.mark.gpu
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-GEMV, TC, AUTO = 1, 2, 0
+GEMV, TC, AUTO, SPLITK, CS = 1, 2, 0, 3, 4
+GEMV_FORMS = [SPLITK, CS]  # the GEMV's two forms, forced
 
 
 def _full(prob, y, what):
@@ -47,7 +49,7 @@ def test_tiny_config(path):
 # ---- config 1 / 2: decode (M=1) and verify (M=16) sets, in full ---------------
 
 @pytest.mark.parametrize("shape", wi.LAYER)
-@pytest.mark.parametrize("path", [AUTO, GEMV, TC])
+@pytest.mark.parametrize("path", [AUTO, GEMV, TC, SPLITK, CS])
 def test_decode_set_m1(shape, path):
     p = wi.generate_named(shape, 1, 1)
     y = Device(p).run(path)
@@ -61,18 +63,23 @@ def test_verify_set_m16(shape):
     _full(p, y, f"verify {shape}")
 
 
-# ---- config 3: prefill M=2048, sampled ----------------------------------------
+# ---- config 3: prefill M=2048, in full ------------------------------------------
 
 @pytest.mark.parametrize("shape", wi.LAYER)
-def test_prefill_m2048_sampled(shape):
+def test_prefill_m2048_full(shape):
+    """Every output of the four projections at M=2048.  For the gate_up shape
+    the same oracle product also checks the fused gate/up kernel: the weights
+    are packed by w4a16_pack_gate_up and y = silu(gate) * up."""
+    import int4_weight_only_gemm_gb300 as w
     p = wi.generate_named(shape, 2048, 3)
     d = Device(p)
-    y = d.run(AUTO)
-    check_sampled(d, y, 4000, seed=3, what=f"prefill {shape}")
-    # two whole rows in full, first and last token
-    rows = np.array([0, 2047])
-    ref = oracle.gemm(p.x[rows], p.qweight, p.scales, p.qzeros)
-    check_close(bf16_to_f64(y[torch.as_tensor(rows, device=y.device)]), ref, f"prefill {shape} rows")
+    ref = oracle.gemm(p.x, p.qweight, p.scales, p.qzeros)
+    check_close(bf16_to_f64(d.run(AUTO)), ref, f"prefill {shape}")
+    if shape == "gate_up":
+        H = p.N // 2
+        qd = w.w4a16_pack_gate_up(d.qw)
+        y = w.w4a16_gemm_gate_up_silu(d.x, qd, d.scales, d.qzeros)
+        check_close(bf16_to_f64(y), oracle.silu_mul(ref, H), "prefill fused gate_up")
 
 
 # ---- config 4: M sweep and the vocabulary shape ------------------------------
@@ -83,7 +90,7 @@ def test_sweep_small_m_both_paths(M, shape):
     p = wi.generate_named(shape, M, 4)
     d = Device(p)
     ref = oracle.gemm(p.x, p.qweight, p.scales, p.qzeros)
-    for path in (GEMV, TC):
+    for path in (GEMV, TC, SPLITK, CS):
         check_close(bf16_to_f64(d.run(path)), ref, f"sweep {shape} M={M} path={path}")
 
 
@@ -94,23 +101,44 @@ def test_sweep_mid_m_full(M, shape):
     _full(p, Device(p).run(AUTO), f"sweep {shape} M={M}")
 
 
-@pytest.mark.parametrize("M", [64, 128, 8192])
+@pytest.mark.parametrize("M", [64, 128])
 @pytest.mark.parametrize("shape", wi.LAYER)
-def test_sweep_large_m_sampled(M, shape):
-    p = wi.generate_named(shape, M, 4)
-    d = Device(p)
-    check_sampled(d, d.run(AUTO), 3000, seed=M, what=f"sweep {shape} M={M}")
+def test_sweep_large_m_full(M, shape):
+    _full(*_run_auto(shape, M, 4), f"sweep {shape} M={M}")
 
 
-@pytest.mark.parametrize("M,path", [(1, GEMV), (1, TC), (16, TC)])
-def test_vocab_shape(M, path):
+def _run_auto(shape, M, seed):
+    p = wi.generate_named(shape, M, seed)
+    return p, Device(p).run(AUTO)
+
+
+def rows_m8192(M=8192, seed=8192):
+    """Whole rows checked at M=8192: every row of the first and the last
+    192-token tile, one seeded row from every other tile, and seeded rows
+    beyond those to make up at least 256."""
+    nt = 192
+    tiles = (M + nt - 1) // nt
+    r = np.random.default_rng(seed)
+    rows = set(range(0, nt)) | set(range((tiles - 1) * nt, M))
+    rows |= {int(t * nt + r.integers(0, nt)) for t in range(1, tiles - 1)}
+    while len(rows) < 400:
+        rows.add(int(r.integers(0, M)))
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("shape", wi.LAYER)
+def test_sweep_m8192_whole_rows(shape):
+    p, y = _run_auto(shape, 8192, 4)
+    rows = rows_m8192()
+    assert len(rows) >= 256
+    ref = oracle.gemm(np.ascontiguousarray(p.x[rows]), p.qweight, p.scales, p.qzeros)
+    check_close(bf16_to_f64(y[torch.as_tensor(rows, device=y.device)]), ref, f"sweep {shape} M=8192 rows")
+
+
+@pytest.mark.parametrize("M,path", [(1, GEMV), (1, SPLITK), (1, TC), (16, TC)])
+def test_vocab_shape_full(M, path):
     p = wi.generate_named("vocab", M, 4)
-    d = Device(p)
-    y = d.run(path)
-    check_sampled(d, y, 6000, seed=5, what=f"vocab M={M} path={path}")
-    rows = np.array([0, M - 1])
-    ref = oracle.gemm(p.x[rows], p.qweight, p.scales, p.qzeros)
-    check_close(bf16_to_f64(y[torch.as_tensor(rows, device=y.device)]), ref, f"vocab M={M} rows")
+    _full(p, Device(p).run(path), f"vocab M={M} path={path}")
 
 
 # ---- edge cases: ragged tiles, odd M, one group --------------------------------
@@ -124,7 +152,7 @@ def test_ragged_and_odd_shapes(M, K, N):
     p = wi.generate(M, K, N, seed=M * 7 + K + N)
     d = Device(p)
     ref = oracle.gemm(p.x, p.qweight, p.scales, p.qzeros)
-    paths = [GEMV, TC] if M <= 8 else [TC]
+    paths = [SPLITK, CS, TC] if M <= 8 else [TC]
     for path in paths:
         check_close(bf16_to_f64(d.run(path)), ref, f"M={M} K={K} N={N} path={path}")
 
@@ -150,7 +178,7 @@ def test_exact_case_bit_exact(M):
     want = oracle.f64_to_bf16(ref)
     assert np.array_equal(oracle.bf16_to_f64(want), ref)  # exact in bf16
     d = Device(p)
-    for path in ([GEMV, TC] if M <= 8 else [TC]):
+    for path in ([SPLITK, CS, TC] if M <= 8 else [TC]):
         got = bf16_bits(d.run(path))
         assert np.array_equal(got, want), f"path {path}: {np.count_nonzero(got != want)} bits differ"
 
@@ -163,15 +191,16 @@ def test_zero_codes_give_zero():
     qz = np.zeros((K // 128, N // 8), np.uint32)
     s = wi.f64_to_f16_bits(r.uniform(0.001, 0.02, (K // 128, N)))
     d = Device(wi.Problem(M, K, N, 128, x, qw, s, qz))
-    for path in (GEMV, TC):
+    for path in (SPLITK, CS, TC):
         y = d.run(path)
         assert torch.count_nonzero(y.float()).item() == 0
 
 
 # ---- determinism, workspace reuse, streams ------------------------------------
 
-@pytest.mark.parametrize("shape,M,path", [("o_proj", 1, GEMV), ("down", 4, GEMV), ("o_proj", 16, TC),
-                                          ("down", 16, TC), ("qkv", 2048, TC)])
+@pytest.mark.parametrize("shape,M,path", [("o_proj", 1, SPLITK), ("down", 4, SPLITK), ("o_proj", 1, CS),
+                                          ("down", 8, CS), ("o_proj", 16, TC), ("down", 16, TC),
+                                          ("qkv", 2048, TC)])
 def test_deterministic_and_workspace_reused(shape, M, path):
     p = wi.generate_named(shape, M, 9)
     d = Device(p)
@@ -250,8 +279,8 @@ def test_one_workspace_across_shapes_and_paths():
     """A single workspace serves any sequence of calls: split-K partial sums
     of one problem must never disturb the arrival counters of the next."""
     import int4_weight_only_gemm_gb300 as w
-    seq = [("down", 16, TC), ("gate_up", 1, GEMV), ("o_proj", 1, GEMV), ("vocab", 1, GEMV),
-           ("qkv", 16, TC), ("gate_up", 4, GEMV)]
+    seq = [("down", 16, TC), ("gate_up", 1, SPLITK), ("o_proj", 1, SPLITK), ("vocab", 1, SPLITK),
+           ("qkv", 16, TC), ("gate_up", 4, SPLITK), ("down", 2, CS)]
     need = max(w.w4a16_workspace_bytes(M, *reversed(wi.shape_kn(s)), path=pth) for s, M, pth in seq)
     ws = w.new_workspace(need)
     for i, (shape, M, path) in enumerate(seq):
@@ -264,8 +293,9 @@ def test_one_workspace_across_shapes_and_paths():
 # ---- launch flags: programmatic dependent launch ------------------------------
 
 @pytest.mark.parametrize("flags", [0, 1, 3])
-@pytest.mark.parametrize("shape,M,path", [("qkv", 1, GEMV), ("down", 8, GEMV), ("o_proj", 16, TC),
-                                          ("gate_up", 64, TC), ("down", 300, TC)])
+@pytest.mark.parametrize("shape,M,path", [("qkv", 1, GEMV), ("down", 8, GEMV), ("qkv", 1, SPLITK),
+                                          ("down", 8, SPLITK), ("o_proj", 16, TC), ("gate_up", 64, TC),
+                                          ("down", 300, TC)])
 def test_launch_flags_same_result(flags, shape, M, path):
     """Every flag combination gives the same bits (the flags change launch
     overlap only) and matches the oracle."""
@@ -278,7 +308,7 @@ def test_launch_flags_same_result(flags, shape, M, path):
     check_sampled(d, y, 1500, seed=2, what=f"flags={flags} {shape} M={M}")
 
 
-@pytest.mark.parametrize("M,path", [(1, GEMV), (4, GEMV), (16, TC), (256, TC)])
+@pytest.mark.parametrize("M,path", [(1, GEMV), (4, GEMV), (1, SPLITK), (2, CS), (16, TC), (256, TC)])
 @pytest.mark.parametrize("flags", [1, 3])
 def test_chained_layers_respect_order(M, path, flags):
     """Layer 2 reads layer 1's output as its x.  Launched back to back as
