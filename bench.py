@@ -476,6 +476,198 @@ def measure_gate_up_silu(w, torch, device, hbm, bf16_peak):
     return out
 
 
+# ---------------------------------------------------------------------------
+# the M sweep (config 4) and the dispatch candidates
+# ---------------------------------------------------------------------------
+
+SWEEP_M = (1, 2, 4, 8, 16, 32, 64, 128, 8192)
+# the dispatch table also measures prefill-sized M between 128 and 8192
+TUNE_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 2048, 8192)
+L2_BYTES = 129 << 20
+PATH_NAMES = {1: "gemv", 2: "tc", 3: "gemv_splitk", 4: "gemv_cs"}
+
+
+def sweep_items(vocab_ms=(1, 16), ms=SWEEP_M):
+    """(shape, M) pairs of the sweep: the four projections at every M of `ms`,
+    the vocabulary head at `vocab_ms`."""
+    items = [(s, m) for m in ms for s in wi.LAYER]
+    return items + [("vocab", m) for m in vocab_ms]
+
+
+def candidates(M):
+    """Kernel configurations the dispatch table chooses from at this M:
+    (name, path, flags); the token tiles the tensor-core kernel may use here."""
+    out = []
+    if M <= 8:
+        out += [("gemv_splitk", 3, 1), ("gemv_cs", 4, 1)]
+    for nt in (16, 32, 64, 128, 192):
+        if nt <= max(16, 2 * M) and (M > 8 or nt == 16) and (M < 2048 or nt >= 64):
+            out.append((f"tc{nt}", 2, 1 | (nt << 8)))
+    return out
+
+
+def time_gemm(w, torch, p, device, path, flags, reps_target_ms=20.0):
+    """Microseconds per launch of one GEMM: a CUDA graph launches it over a
+    rotation of weight copies whose total exceeds twice the L2 (so every
+    launch streams its weights from HBM), replayed after a warm-up."""
+    x, qw, sc, qz = w.to_device(p, device)
+    qd = w.w4a16_pack(qw)
+    del qw
+    wbytes = p.K * p.N // 2
+    copies = int(min(64, max(2, -(-int(2.1 * L2_BYTES) // wbytes))))
+    qds = [qd] + [qd.clone() for _ in range(copies - 1)]
+    y = torch.empty((p.M, p.N), dtype=torch.bfloat16, device=device)
+    ws = w.new_workspace(w.w4a16_workspace_bytes_max(p.M, p.N, p.K), device)
+    nbytes = ws.numel()
+
+    def launch_all(stream_ptr):
+        for q in qds:
+            st = w.w4a16_gemm_raw(x.data_ptr(), q.data_ptr(), sc.data_ptr(), qz.data_ptr(), p.M, p.N, p.K, 128,
+                                  y.data_ptr(), ws.data_ptr(), nbytes, path, stream_ptr, flags)
+            if st != 0:
+                raise RuntimeError(f"w4a16_gemm path {path} flags {flags}: {w.w4a16_status_str(st)}")
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        launch_all(s.cuda_stream)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        launch_all(torch.cuda.current_stream().cuda_stream)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    once = max(e0.elapsed_time(e1), 1e-3)
+    reps = int(max(2, min(200, reps_target_ms / once)))
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * copies)
+    del g, qds, qd, x, y, ws
+    return us, copies
+
+
+def roofline_us(M, K, N, hbm, bf16_peak):
+    return max(gemm_bytes(M, K, N) / (hbm * 1e3), gemm_flops(M, K, N) / (bf16_peak * 1e6))
+
+
+def measure_sweep(w, torch, device, hbm, bf16_peak):
+    """Config 4: every (shape, M) of the sweep through the library's own
+    kernel choice (path AUTO); per GEMM us, GB/s, TFLOP/s and the fraction of
+    the roofline max(bytes / HBM, flops / bf16 peak), and the sums over the
+    four projections of a layer."""
+    out = {}
+    for shape, M in sweep_items():
+        p = wi.generate_named(shape, M, 4)
+        us, copies = time_gemm(w, torch, p, device, 0, 1)
+        rl = roofline_us(M, p.K, p.N, hbm, bf16_peak)
+        e = out.setdefault(f"M={M}", {})
+        e[shape] = {"us": us, "GB/s": gemm_bytes(M, p.K, p.N) / us / 1e3,
+                    "TFLOP/s": gemm_flops(M, p.K, p.N) / us / 1e6, "frac": rl / us,
+                    "path": PATH_NAMES.get(w.w4a16_auto_path(M, p.N, p.K), "?"), "weight_copies": copies}
+        torch.cuda.empty_cache()
+    for key, e in out.items():
+        M = int(key[2:])
+        if all(s in e for s in wi.LAYER):
+            us = sum(e[s]["us"] for s in wi.LAYER)
+            rl = sum(roofline_us(M, *wi.shape_kn(s), hbm, bf16_peak) for s in wi.LAYER)
+            e["layer"] = {"us": us, "frac": rl / us}
+    return out
+
+
+def tune_dispatch(path_out, ms=TUNE_M):
+    """Times every dispatch candidate at every point of the sweep (the vocabulary
+    head at M <= 128 as well) and writes the measurements that
+    int4_weight_only_gemm_gb300/csrc/gen_dispatch.py turns into the table."""
+    import torch
+    import int4_weight_only_gemm_gb300 as w
+    w.load_library()
+    device = torch.device("cuda", 0)
+    props = torch.cuda.get_device_properties(device)
+    entries = []
+    for shape, M in sweep_items(vocab_ms=tuple(m for m in (1, 2, 4, 8, 16, 32, 64, 128) if m in ms), ms=ms):
+        p = wi.generate_named(shape, M, 4)
+        for name, path, flags in candidates(M):
+            us, _ = time_gemm(w, torch, p, device, path, flags)
+            entries.append({"shape": shape, "K": p.K, "N": p.N, "M": M, "config": name, "us": round(us, 3)})
+            print(json.dumps(entries[-1]), flush=True)
+        torch.cuda.empty_cache()
+    doc = {"what": "microseconds per launch of each dispatch candidate (CUDA graphs over rotating weight copies "
+                   "> 2x L2); written by bench.py --tune-dispatch",
+           "device": props.name, "sms": props.multi_processor_count,
+           "when": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime()), "entries": entries}
+    with open(path_out, "w") as f:
+        json.dump(doc, f, indent=1)
+
+
+
+def measure_swa(w, torch, device, hbm, bf16_peak):
+    """Sliding-window decode attention of the drafter on the long scenario's
+    context (8192 prompt + 256 generated = 8448 positions), window 1024 and
+    2048, a 16-token draft block and a single query; 32 query heads over 8
+    key/value heads of width 128.  CUDA graphs over 8 copies of the caches
+    (277 MB, more than twice the L2).  Algorithmic bytes: the keys and values
+    of every head's window once, plus q and out; flops 4 * 128 per (query,
+    head, visible key)."""
+    Hq, Hkv, d, L = 32, 8, 128, 8448
+    out = {}
+    r = np.random.default_rng(12)
+    kc = [torch.randn((Hkv, L, d), device=device).to(torch.bfloat16) for _ in range(COPIES)]
+    vt = [torch.randn((Hkv, d, L), device=device).to(torch.bfloat16) for _ in range(COPIES)]
+    for nq in (16, 1):
+        q = torch.from_numpy(r.standard_normal((nq, Hq, d), dtype=np.float32)).to(device).to(torch.bfloat16)
+        o = torch.empty_like(q)
+        for W in (1024, 2048):
+            ws = w.new_workspace(w.w4a16_swa_workspace_bytes(nq, Hq, Hkv, L, W), device)
+
+            def launch_all():
+                for c in range(COPIES):
+                    w.w4a16_swa_attention(q, kc[c], vt[c], L, W, False, out=o, workspace=ws)
+
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                launch_all()
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                launch_all()
+            for _ in range(5):
+                g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 200
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (reps * COPIES)
+            keys = min(L, W + nq - 1)                      # the block's window, per key/value head
+            visible = sum(min(W, L - nq + i + 1) for i in range(nq))  # keys seen by each query
+            nbytes = Hkv * keys * d * 2 * 2 + 2 * nq * Hq * d * 2
+            flops = 4 * d * visible * Hq
+            rl = max(nbytes / (hbm * 1e3), flops / (bf16_peak * 1e6))
+            out[f"nq={nq} W={W}"] = {"us": us, "GB/s": nbytes / us / 1e3, "TFLOP/s": flops / us / 1e6,
+                                     "frac": rl / us, "bytes": nbytes, "flops": flops,
+                                     "bound": "hbm" if nbytes / hbm > flops / bf16_peak * 1e-3 else "tensor"}
+            del g, ws
+        del q, o
+    del kc, vt
+    torch.cuda.empty_cache()
+    out["shape"] = f"Hq={Hq}, Hkv={Hkv}, d={d}, L={L}, causal; value cache transposed per head"
+    return out
+
+
 def max_over_ranks(dist, torch, value: float, device) -> float:
     """The largest of the ranks' values (the slowest rank's time); the value
     itself without a process group."""
@@ -522,9 +714,17 @@ def main():
                     help="SHAPE:M[:PATH] -- run that one GEMM --reps times and exit (for profilers); "
                          "PATH 0 = auto, 1 = split-K GEMV, 2 = tensor-core kernel")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--no-sweep", action="store_true", help="skip the M sweep")
+    ap.add_argument("--tune-dispatch", default="",
+                    help="OUT.json -- time every dispatch candidate over the sweep, write them and exit")
+    ap.add_argument("--tune-m", default="", help="comma-separated M values for --tune-dispatch (default: all)")
     args = ap.parse_args()
     if args.case:
         run_case(args.case, args.reps)
+        return
+    if args.tune_dispatch:
+        ms = tuple(int(v) for v in args.tune_m.split(",")) if args.tune_m else TUNE_M
+        tune_dispatch(args.tune_dispatch, ms)
         return
     if args.warmup < 3:
         args.warmup = 3
@@ -576,7 +776,19 @@ def main():
     value = wl.bytes * args.steps * world / (ms / 1e3) / 1e9
 
     extra = {}
-    if rank == 0 and not args.no_extra:
+    failed = []  # extras that raised: the error goes into the line, later GPU extras are skipped
+
+    def guarded(name, fn):
+        if failed:
+            extra[name] = {"skipped": f"after the failure of {failed[0]}"}
+            return
+        try:
+            fn()
+        except Exception as exc:  # a CUDA error leaves the context unusable: stop all GPU work
+            failed.append(name)
+            extra[name] = {"error": repr(exc)[:400]}
+
+    def ex_decode_per_gemm():
         # each projection alone (graph of the 8-copy rotation of that GEMM)
         per = {}
         for i, g in enumerate(wl.gemms):
@@ -587,6 +799,8 @@ def main():
             per[g["shape"]] = {"us": t_ms / n * 1e3, "GB/s": b * n / (t_ms / 1e3) / 1e9,
                                "frac": b * n / (t_ms / 1e3) / 1e9 / hbm}
         extra["decode_m1_per_gemm"] = per
+
+    def ex_decode_flags():
         # the decode set under each launch-flag combination
         fl = {}
         for flags, name in ((0, "plain"), (1, "pdl"), (3, "pdl_static_weights")):
@@ -595,36 +809,36 @@ def main():
             t_ms = time_graph_steps(torch, ps, rt, COPIES, n, 50)
             fl[name] = {"us_per_step": t_ms / n * 1e3, "GB/s": wl.bytes * n / (t_ms / 1e3) / 1e9}
         extra["decode_m1_flags"] = fl
-        for name, unit in (("verify_m16", "GB/s"), ("prefill_m2048", "TFLOP/s")):
-            seed, items = wi.WORKLOADS[name]
-            small = unit == "GB/s"
-            copies = COPIES if small else 2
-            wl2 = Workload(w, torch, items, seed, copies, device)
-            ps, rt = wl2.graphs()
-            n = 4000 if small else 40
-            t_ms = time_graph_steps(torch, ps, rt, copies, n, 10)
-            if unit == "GB/s":
-                v = wl2.bytes * n / (t_ms / 1e3) / 1e9
-                frac = v / hbm
-            else:
-                v = wl2.flops * n / (t_ms / 1e3) / 1e12
-                frac = v / bf16_peak
-            per2 = {}
-            for i, g in enumerate(wl2.gemms):
-                ps1, rt1 = wl2.graphs(only=i)
-                n1 = 2000 if small else 20
-                t1 = time_graph_steps(torch, ps1, rt1, copies, n1, 5)
-                per2[g["shape"]] = {"us": t1 / n1 * 1e3,
-                                    "GB/s": gemm_bytes(g["M"], g["K"], g["N"]) * n1 / (t1 / 1e3) / 1e9,
-                                    "TFLOP/s": gemm_flops(g["M"], g["K"], g["N"]) * n1 / (t1 / 1e3) / 1e12}
-            extra[name] = {"value": v, "unit": unit, "frac": frac, "ms_per_step": t_ms / n,
-                           "workload": ", ".join(f"{s} M={M}" for s, M in items), "per_gemm": per2}
-            del wl2, ps, rt
-            torch.cuda.empty_cache()
 
-    if rank == 0 and not args.no_extra:
-        extra["requant_pack_gate_up"] = measure_requant(w, torch, device, hbm)
-        extra["gate_up_silu"] = measure_gate_up_silu(w, torch, device, hbm, bf16_peak)
+    def ex_workload(name, unit):
+        seed, items = wi.WORKLOADS[name]
+        small = unit == "GB/s"
+        copies = COPIES if small else 2
+        wl2 = Workload(w, torch, items, seed, copies, device)
+        ps, rt = wl2.graphs()
+        n = 4000 if small else 40
+        t_ms = time_graph_steps(torch, ps, rt, copies, n, 10)
+        if unit == "GB/s":
+            v = wl2.bytes * n / (t_ms / 1e3) / 1e9
+            frac = v / hbm
+        else:
+            v = wl2.flops * n / (t_ms / 1e3) / 1e12
+            frac = v / bf16_peak
+        per2 = {}
+        for i, g in enumerate(wl2.gemms):
+            ps1, rt1 = wl2.graphs(only=i)
+            n1 = 2000 if small else 20
+            t1 = time_graph_steps(torch, ps1, rt1, copies, n1, 5)
+            per2[g["shape"]] = {"us": t1 / n1 * 1e3,
+                                "GB/s": gemm_bytes(g["M"], g["K"], g["N"]) * n1 / (t1 / 1e3) / 1e9,
+                                "TFLOP/s": gemm_flops(g["M"], g["K"], g["N"]) * n1 / (t1 / 1e3) / 1e12}
+            del ps1, rt1
+        extra[name] = {"value": v, "unit": unit, "frac": frac, "ms_per_step": t_ms / n,
+                       "workload": ", ".join(f"{s} M={M}" for s, M in items), "per_gemm": per2}
+        del ps, rt, wl2
+        torch.cuda.empty_cache()
+
+    def ex_verify_batched():
         # batched speculative verify: b draft blocks of 16 tokens through the
         # four projections of the layer, PDL-chained in one graph per step
         vb = {}
@@ -637,12 +851,27 @@ def main():
             us = t_ms / n * 1e3
             vb[f"M={M}"] = {"us_per_step": us, "GB/s": wl3.bytes / us / 1e3, "frac": wl3.bytes / us / 1e3 / hbm,
                             "tokens/s": M / us * 1e6}
-            del wl3, ps, rt
+            del ps, rt, wl3
             torch.cuda.empty_cache()
         extra["verify_batched"] = vb
 
+    if rank == 0 and not args.no_extra:
+        guarded("decode_m1_per_gemm", ex_decode_per_gemm)
+        guarded("decode_m1_flags", ex_decode_flags)
+        guarded("verify_m16", lambda: ex_workload("verify_m16", "GB/s"))
+        guarded("prefill_m2048", lambda: ex_workload("prefill_m2048", "TFLOP/s"))
+        guarded("requant_pack_gate_up",
+                lambda: extra.__setitem__("requant_pack_gate_up", measure_requant(w, torch, device, hbm)))
+        guarded("gate_up_silu", lambda: extra.__setitem__(
+            "gate_up_silu", measure_gate_up_silu(w, torch, device, hbm, bf16_peak)))
+        guarded("verify_batched", ex_verify_batched)
+        guarded("swa_decode_attention",
+                lambda: extra.__setitem__("swa_decode_attention", measure_swa(w, torch, device, hbm, bf16_peak)))
+        if not args.no_sweep:
+            guarded("sweep", lambda: extra.__setitem__("sweep", measure_sweep(w, torch, device, hbm, bf16_peak)))
+
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not failed:
         e2e_v, h2d, d2h, e2e_ms = measure_e2e(w, torch, wl, min(2000, max(50, args.steps // 10)))
         e2e = {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms, "api": "int4_weight_only_gemm_gb300.w4a16_gemm (C ABI w4a16_gemm_path)"}

@@ -181,7 +181,13 @@ enum {
      * written by work still in flight on the stream (true for a model whose
      * weights were packed earlier), so the kernel may start streaming them
      * before the preceding work completes. */
-    W4A16_FLAG_STATIC_WEIGHTS = 1u << 1
+    W4A16_FLAG_STATIC_WEIGHTS = 1u << 1,
+    /* Tuning: bits 8..15 hold a token-tile width (16, 32, 64, 128 or 192)
+     * that the tensor-core kernel uses instead of its dispatch table's choice;
+     * 0 keeps the table.  Other values give W4A16_EINVAL.  The split-K
+     * workspace depends on the tile: size it with w4a16_workspace_bytes_max. */
+    W4A16_FLAG_TOKEN_TILE_SHIFT = 8,
+    W4A16_FLAG_TOKEN_TILE_MASK = 0xFFu << 8
 };
 
 /* As w4a16_gemm_path with explicit launch flags (W4A16_EINVAL for unknown bits). */
@@ -284,6 +290,47 @@ int w4a16_selftest_wait_timeout(long long wait_ns, w4a16_stream_t stream);
 int w4a16_gemm_noalloc(const void *x, const uint32_t *qweight_dev, const void *scales,
                        const uint32_t *qzeros, int M, int N, int K, int group, void *y,
                        w4a16_stream_t stream);
+
+/*
+ * Sliding-window decode attention of the drafter ("Quantize the Target,
+ * Quantize the Drafter", pith.science review, "Assumptions & free
+ * parameters": SWA window length 1024 on the leaderboard, 1024 or 2048 after
+ * the latency / acceptance trade-off; DFlash block size 16; the gptget.net
+ * summary: sliding-window attention reduces long-context decoding latency):
+ * a block of nq query tokens at positions L-nq .. L-1 attends, per query head
+ * h, to the keys and values of head hk = h / (Hq / Hkv) in its window
+ *
+ *     J_i = [max(0, e_i - window + 1), e_i],  e_i = L - nq + i (block = 0, causal)
+ *                                             e_i = L - 1      (block = 1)
+ *     out[i][h] = sum_{j in J_i} softmax_j(q[i][h] . k[hk][j] / sqrt(128)) v[hk][j]
+ *
+ * with scores and the softmax in f32 (the weights rounded once to bf16 for
+ * the tensor-core product with v), the sum in f32, the result rounded to bf16.
+ *
+ *   q          bf16 [nq][Hq][128], device
+ *   k_cache    bf16 [Hkv][Lmax][128], device: row j = key of position j
+ *   vt_cache   bf16 [Hkv][128][Lmax], device: the values, transposed per head
+ *              (column j = value of position j), so that both products of the
+ *              kernel read operands contiguous along their reduction axis
+ *   out        bf16 [nq][Hq][128], device, fully written
+ *   head_dim   128 (W4A16_EUNSUPPORTED otherwise); Hq % Hkv == 0;
+ *              nq * Hq / Hkv <= 128 (W4A16_EUNSUPPORTED); 1 <= nq <= L <= Lmax;
+ *              Lmax % 8 == 0; window >= 1; block 0 or 1 (W4A16_EINVAL)
+ *   workspace  caller-owned, zero-filled once, w4a16_swa_workspace_bytes bytes
+ *              (W4A16_EWORKSPACE if missing or short); each call leaves its
+ *              counters at zero again
+ *   flags      0 or W4A16_FLAG_PDL
+ *
+ * All pointers 16-byte aligned (W4A16_EALIGN); out may not overlap the
+ * inputs (W4A16_EINVAL).  Asynchronous on `stream`; only positions < L of the
+ * caches are read.
+ */
+int w4a16_swa_attention(const void *q, const void *k_cache, const void *vt_cache, int nq, int Hq, int Hkv,
+                        int head_dim, int L, int Lmax, int window, int block, void *out, void *workspace,
+                        size_t workspace_bytes, unsigned flags, w4a16_stream_t stream);
+
+/* Workspace bytes of w4a16_swa_attention for these sizes (0 for invalid ones). */
+size_t w4a16_swa_workspace_bytes(int nq, int Hq, int Hkv, int head_dim, int L, int window, int block);
 
 /* Number of kernel launches the library has issued in this process (every
  * entry point that launches counts its kernel; w4a16_gemm_noalloc's counter

@@ -78,6 +78,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.w4a16_status_str.restype = ctypes.c_char_p
             lib.w4a16_last_device_status.argtypes = [vp]
             lib.w4a16_launch_count.restype = ctypes.c_uint64
+            lib.w4a16_swa_attention.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, ci, vp, vp, sz,
+                                                ctypes.c_uint, vp]
+            lib.w4a16_swa_workspace_bytes.argtypes = [ci, ci, ci, ci, ci, ci, ci]
+            lib.w4a16_swa_workspace_bytes.restype = sz
             _lib = lib
     return _lib
 
@@ -314,6 +318,42 @@ def w4a16_last_device_status(stream=None) -> int:
 
 def w4a16_launch_count() -> int:
     return int(load_library().w4a16_launch_count())
+
+
+def w4a16_swa_workspace_bytes(nq: int, Hq: int, Hkv: int, L: int, window: int, block: bool = False,
+                              head_dim: int = 128) -> int:
+    return int(load_library().w4a16_swa_workspace_bytes(nq, Hq, Hkv, head_dim, L, window, int(block)))
+
+
+def w4a16_swa_attention(q: torch.Tensor, k_cache: torch.Tensor, vt_cache: torch.Tensor, L: int, window: int,
+                        block: bool = False, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                        stream=None, flags: int = FLAG_PDL) -> torch.Tensor:
+    """Sliding-window decode attention of a block of nq queries at positions
+    L-nq .. L-1 (see include/w4a16.h).
+
+    q [nq, Hq, 128] bf16; k_cache [Hkv, Lmax, 128] bf16; vt_cache [Hkv, 128,
+    Lmax] bf16 (values transposed per head); returns out [nq, Hq, 128] bf16."""
+    _check(q, "q", torch.bfloat16)
+    _check(k_cache, "k_cache", torch.bfloat16)
+    _check(vt_cache, "vt_cache", torch.bfloat16)
+    if q.dim() != 3 or k_cache.dim() != 3 or vt_cache.dim() != 3:
+        raise ValueError("q, k_cache, vt_cache must be 3-D")
+    nq, Hq, d = q.shape
+    Hkv, Lmax, _ = k_cache.shape
+    if tuple(vt_cache.shape) != (Hkv, d, Lmax):
+        raise ValueError(f"vt_cache has shape {tuple(vt_cache.shape)}, expected {(Hkv, d, Lmax)}")
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, q.shape)
+    lib = load_library()
+    need = int(lib.w4a16_swa_workspace_bytes(nq, Hq, Hkv, d, L, window, int(block)))
+    if workspace is None:
+        workspace = _cached_workspace(max(need, 1), q.device)
+    st = lib.w4a16_swa_attention(q.data_ptr(), k_cache.data_ptr(), vt_cache.data_ptr(), nq, Hq, Hkv, d, L, Lmax,
+                                 window, int(block), out.data_ptr(), workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), flags, _stream(stream))
+    _raise(st, "w4a16_swa_attention")
+    return out
 
 
 def to_device(problem, device="cuda"):

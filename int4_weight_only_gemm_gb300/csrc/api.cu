@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "dispatch_table.h"
 #include "kernels.h"
 
 namespace w4a16 {
@@ -85,18 +86,18 @@ bool gemv_uses_cs(int M, int N, int K, int sms, int guH, GemvCsPlan* cp) {
            (long long)K * N / 2 <= kCsMaxCtaBytes * cp->ctas;
 }
 
-// Kernel choice per M, from measured times on GB300 (layer shapes of a ~4B
-// decoder, M = 1..8): the GEMV's arithmetic grows with M while the
-// tensor-core kernel's time is flat in M, and they cross between M = 2 and
-// M = 4, later for smaller weight matrices.  GEMV when M <= 2, or M <= 4 with
-// at most 16M weights, and it fits in shared memory; the tensor-core GEMM
-// otherwise.
+// Kernel choice for AUTO: the dispatch table's row (measured on GB300 over
+// the decoder's shapes, see dispatch_table.h), provided the GEMV it names can
+// run this problem; the tensor-core kernel otherwise.
 int choose_path(int M, int N, int K, int sms) {
+    const DispatchRow* r = dispatch_row(M, K, N);
     GemvPlan gp;
     GemvCsPlan cp;
-    const bool small = (long long)K * N <= (16ll << 20);
-    if ((M <= 2 || (M <= 4 && small)) && (gemv_cs_plan(M, N, K, sms, 0, &cp) || gemv_plan(M, N, K, sms, &gp)))
-        return W4A16_PATH_GEMV;
+    if (r && M <= 8) {
+        if (r->path == W4A16_PATH_GEMV_CS && gemv_cs_plan(M, N, K, sms, 0, &cp)) return W4A16_PATH_GEMV_CS;
+        if ((r->path == W4A16_PATH_GEMV_CS || r->path == W4A16_PATH_GEMV_SPLITK) && gemv_plan(M, N, K, sms, &gp))
+            return W4A16_PATH_GEMV_SPLITK;
+    }
     return W4A16_PATH_TC;
 }
 
@@ -119,7 +120,7 @@ size_t ws_for_path(int path, int M, int N, int K, int sms) {
 // launch, which changes no ordering (every kernel waits for the preceding grid
 // before it touches global memory) but lets its launch overlap that grid's end.
 constexpr unsigned kDefaultFlags = W4A16_FLAG_PDL;
-constexpr unsigned kKnownFlags = W4A16_FLAG_PDL | W4A16_FLAG_STATIC_WEIGHTS;
+constexpr unsigned kKnownFlags = W4A16_FLAG_PDL | W4A16_FLAG_STATIC_WEIGHTS | W4A16_FLAG_TOKEN_TILE_MASK;
 
 // guH > 0: fused gate/up weights with N = 2 guH columns, y = silu(gate) * up of [M][guH]
 int run_gemm(int path, unsigned flags, const void* x, const uint32_t* qd, const void* scales, const uint32_t* qzeros,
@@ -147,7 +148,10 @@ int run_gemm(int path, unsigned flags, const void* x, const uint32_t* qd, const 
                         static_cast<uint16_t*>(y), M, N, K, ws, gp, stream, flags, guH);
     } else if (path == W4A16_PATH_TC) {
         TcPlan tp;
-        if (!tc_plan(M, N, K, sms, &tp)) return W4A16_EUNSUPPORTED;
+        const int force_nt = (int)((flags & W4A16_FLAG_TOKEN_TILE_MASK) >> W4A16_FLAG_TOKEN_TILE_SHIFT);
+        if (force_nt && force_nt != 16 && force_nt != 32 && force_nt != 64 && force_nt != 128 && force_nt != 192)
+            return W4A16_EINVAL;
+        if (!tc_plan(M, N, K, sms, &tp, force_nt)) return W4A16_EUNSUPPORTED;
         if (tp.ws_bytes && (!ws || ws_bytes < tp.ws_bytes || !aligned16(ws))) return W4A16_EWORKSPACE;
         e = launch_tc(static_cast<const uint16_t*>(x), qd, static_cast<const uint16_t*>(scales), qzeros,
                       static_cast<uint16_t*>(y), M, N, K, ws, tp, stream, flags, guH);
@@ -181,6 +185,24 @@ int check_gemm(const void* x, const uint32_t* qd, const void* scales, const uint
 }
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+const DispatchRow* dispatch_row(int M, int K, int N) {
+    const long long kn = (long long)K * N;
+    int cls = 0;
+    while (cls < kDispatchClasses - 1 && kn > kClassMaxWeights[cls]) ++cls;
+    const DispatchRow* last = nullptr;
+    for (const DispatchRow& r : kDispatch) {
+        if (r.cls != cls) continue;
+        last = &r;
+        if (M <= r.m_max) return &r;
+    }
+    return last;  // beyond the sweep: the largest M measured
+}
+
+int dispatch_nt(int M, int K, int N) {
+    const DispatchRow* r = dispatch_row(M, K, N);
+    return r && r->path == W4A16_PATH_TC ? r->nt : 0;
+}
 
 }  // namespace w4a16
 
@@ -275,6 +297,15 @@ size_t w4a16_workspace_bytes_max(int max_M, int N, int K, int group) {
             size_t b = w4a16_workspace_bytes_path(path, m, N, K, group);
             if (b > best) best = b;
         }
+        // every token tile the tuning flag can force
+        const int dev = current_device();
+        const int sms = dev >= 0 ? device_sms(dev) : 0;
+        if (sms > 0 && group == 128 && check_kn(N, K) == W4A16_OK) {
+            for (int nt : {16, 32, 64, 128, 192}) {
+                TcPlan tp;
+                if (tc_plan(m, N, K, sms, &tp, nt) && tp.ws_bytes > best) best = tp.ws_bytes;
+            }
+        }
     }
     return best;
 }
@@ -351,15 +382,58 @@ int w4a16_last_device_status(w4a16_stream_t stream) {
     const int a = gemv_read_status();
     const int b = tc_read_status();
     const int c = selftest_read_status();
-    if (a == W4A16_ECUDA || b == W4A16_ECUDA || c == W4A16_ECUDA) return W4A16_ECUDA;
+    const int d = swa_read_status();
+    if (a == W4A16_ECUDA || b == W4A16_ECUDA || c == W4A16_ECUDA || d == W4A16_ECUDA) return W4A16_ECUDA;
     if (a != 0) return a;
     if (b != 0) return b;
+    if (d != 0) return d;
     return c;
 }
 
 int w4a16_selftest_wait_timeout(long long wait_ns, w4a16_stream_t stream) {
     if (wait_ns < 1000 || wait_ns > 1000000000ll) return W4A16_EINVAL;
     if (launch_selftest_wait((uint64_t)wait_ns, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return W4A16_ECUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return W4A16_OK;
+}
+
+static int check_swa(int nq, int Hq, int Hkv, int head_dim, int L, int Lmax, int window, int block) {
+    if (nq < 1 || Hq < 1 || Hkv < 1 || L < nq || Lmax < L || window < 1 || (block != 0 && block != 1))
+        return W4A16_EINVAL;
+    if (Hq % Hkv != 0 || Lmax % 8 != 0) return W4A16_EINVAL;
+    if (head_dim != 128) return W4A16_EUNSUPPORTED;
+    if ((long long)nq * (Hq / Hkv) > 128 || Hkv > 65535) return W4A16_EUNSUPPORTED;
+    return W4A16_OK;
+}
+
+size_t w4a16_swa_workspace_bytes(int nq, int Hq, int Hkv, int head_dim, int L, int window, int block) {
+    if (check_swa(nq, Hq, Hkv, head_dim, L, (L + 7) & ~7, window, block) != W4A16_OK) return 0;
+    SwaPlan sp;
+    if (!swa_plan(nq, Hq, Hkv, L, window, block, &sp)) return 0;
+    return sp.ws_bytes;
+}
+
+int w4a16_swa_attention(const void* q, const void* k_cache, const void* vt_cache, int nq, int Hq, int Hkv,
+                        int head_dim, int L, int Lmax, int window, int block, void* out, void* workspace,
+                        size_t workspace_bytes, unsigned flags, w4a16_stream_t stream) {
+    if (!q || !k_cache || !vt_cache || !out) return W4A16_EINVAL;
+    if (flags & ~(unsigned)W4A16_FLAG_PDL) return W4A16_EINVAL;
+    int st = check_swa(nq, Hq, Hkv, head_dim, L, Lmax, window, block);
+    if (st != W4A16_OK) return st;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(vt_cache) || !aligned16(out)) return W4A16_EALIGN;
+    const size_t qbytes = (size_t)nq * Hq * head_dim * 2;
+    const size_t cbytes = (size_t)Hkv * Lmax * head_dim * 2;
+    if (overlaps(out, qbytes, q, qbytes) || overlaps(out, qbytes, k_cache, cbytes) ||
+        overlaps(out, qbytes, vt_cache, cbytes))
+        return W4A16_EINVAL;
+    SwaPlan sp;
+    if (!swa_plan(nq, Hq, Hkv, L, window, block, &sp)) return W4A16_EUNSUPPORTED;
+    if (!workspace || workspace_bytes < sp.ws_bytes || !aligned16(workspace)) return W4A16_EWORKSPACE;
+    if (launch_swa(static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k_cache),
+                   static_cast<const uint16_t*>(vt_cache), static_cast<uint16_t*>(out), nq, Hq, Hkv, L, Lmax, window,
+                   block, workspace, sp, reinterpret_cast<cudaStream_t>(stream), (flags & W4A16_FLAG_PDL) != 0) !=
+        cudaSuccess)
         return W4A16_ECUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return W4A16_OK;

@@ -613,11 +613,11 @@ __global__ void __launch_bounds__(TcCfg<NT, HALF>::kThreads, TcCfg<NT, HALF>::kM
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// Token tile.  An MMA of N <= 128 takes about as long as one of N = 128
-// (~47 ns for M = 128, K = 16, measured), while N = 256 runs at the full rate,
-// so large M takes 192-token tiles: two D buffers of 192 columns still fit
-// beside two A buffers in the 512 tensor-memory columns.  Up to 256 tokens
-// the shorter per-group chain of 128-token tiles measured faster.
+// Token tile when neither the caller nor the dispatch table names one.  An
+// MMA of N <= 128 takes about as long as one of N = 128 (~47 ns for M = 128,
+// K = 16, measured), while N = 256 runs at the full rate, so large M takes
+// 192-token tiles: two D buffers of 192 columns still fit beside two A
+// buffers in the 512 tensor-memory columns.
 static int tc_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 256 ? 128 : 192; }
 // Token tiles of up to kTcHalfMaxNT tokens run the half-SM configuration,
 // two CTAs per SM.  Off: measured at M = 16 and 32 on the decoder's shapes it
@@ -625,10 +625,13 @@ static int tc_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M 
 // engine, which the three copies per group already keep busy.
 constexpr int kTcHalfMaxNT = 0;
 
-bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
+bool tc_plan(int M, int N, int K, int sms, TcPlan* out, int force_nt) {
     const Layout L(K, N);
     const int G = K / 128;
-    const int NT = tc_nt(M);
+    if (force_nt && force_nt != 16 && force_nt != 32 && force_nt != 64 && force_nt != 128 && force_nt != 192)
+        return false;
+    const int table_nt = force_nt ? 0 : dispatch_nt(M, K, N);
+    const int NT = force_nt ? force_nt : table_nt ? table_nt : tc_nt(M);
     const int MT = (M + NT - 1) / NT;
     const bool half = NT <= kTcHalfMaxNT;
     const long long slots = half ? 2ll * sms : sms;  // CTAs resident at once

@@ -31,6 +31,13 @@ int check_gemm(const void* x, const uint32_t* qd, const void* scales, const uint
 // Counts one kernel launch in w4a16_launch_count (api.cu).
 void note_launch();
 
+// The dispatch table's row for this problem (api.cu; dispatch_table.h):
+// path is W4A16_PATH_GEMV_SPLITK, W4A16_PATH_GEMV_CS or W4A16_PATH_TC, nt the
+// tensor-core token tile (0 for the GEMV).
+struct DispatchRow;
+const DispatchRow* dispatch_row(int M, int K, int N);
+int dispatch_nt(int M, int K, int N);  // the table's token tile when it picks the tensor cores, else 0
+
 // guH = 0: plain layout; guH = H: fused gate/up weights with N = 2H columns
 cudaError_t launch_pack(const uint32_t* q, uint32_t* qd, int K, int N, int guH, cudaStream_t s);
 cudaError_t launch_unpack(const uint32_t* qd, uint32_t* q, int K, int N, int guH, cudaStream_t s);
@@ -72,7 +79,8 @@ struct TcPlan {
     bool half;               // the half-SM configuration, two CTAs per SM
     size_t smem, ws_bytes;
 };
-bool tc_plan(int M, int N, int K, int sms, TcPlan* out);
+// force_nt: a token tile (16, 32, 64, 128 or 192) in place of the table's, 0 = the table's
+bool tc_plan(int M, int N, int K, int sms, TcPlan* out, int force_nt = 0);
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
                       uint16_t* y, int M, int N, int K, void* ws, const TcPlan& plan, cudaStream_t s,
                       unsigned flags, int guH);
@@ -95,6 +103,18 @@ cudaError_t launch_kernel(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStr
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 int tc_read_status();
+
+// sliding-window decode attention (head width 128)
+struct SwaPlan {
+    int j0, C;       // first key (a multiple of 8) and 128-key chunks of the block's window
+    int G, R;        // query heads per key / value head; query rows per head group (nq G)
+    size_t ws_bytes;  // the arrival counters, then the f32 partials
+};
+bool swa_plan(int nq, int Hq, int Hkv, int L, int W, int block, SwaPlan* out);
+cudaError_t launch_swa(const uint16_t* q, const uint16_t* kc, const uint16_t* vtc, uint16_t* out, int nq, int Hq,
+                       int Hkv, int L, int Lmax, int W, int block, void* ws, const SwaPlan& plan, cudaStream_t s,
+                       bool pdl);
+int swa_read_status();
 
 // failure-detection self-test
 cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t s);

@@ -331,12 +331,31 @@ def test_chained_layers_respect_order(M, path, flags):
     assert w.w4a16_last_device_status() == 0
 
 
-def test_auto_path_follows_the_measured_rule():
-    """AUTO: GEMV for M <= 2, and M <= 4 when K*N <= 16M; tensor cores otherwise."""
+def _dispatch_rows():
+    """Rows of the generated dispatch table (int4_weight_only_gemm_gb300/csrc/dispatch_table.h)."""
+    import re
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "int4_weight_only_gemm_gb300",
+                       "csrc", "dispatch_table.h")
+    text = open(hdr).read()
+    paths = {"W4A16_PATH_GEMV_SPLITK": SPLITK, "W4A16_PATH_GEMV_CS": CS, "W4A16_PATH_TC": TC}
+    rows = [(int(c), int(m), paths[p], int(nt)) for c, m, p, nt in
+            re.findall(r"\{(\d+), (\d+), (W4A16_PATH_\w+), (\d+)\}", text)]
+    limits = [int(v) for v in re.search(r"kClassMaxWeights\[\] = \{([^}]*)\}", text).group(1)
+              .replace("ll", "").split(",")]
+    return rows, limits
+
+
+def test_auto_path_follows_the_dispatch_table():
+    """AUTO picks the generated table's kernel for every shape of the decoder
+    and the vocabulary head, at M inside and between the measured points."""
     import int4_weight_only_gemm_gb300 as w
-    for M, shape, want in [(1, "gate_up", w.PATH_GEMV), (2, "down", w.PATH_GEMV), (3, "qkv", w.PATH_GEMV),
-                           (4, "o_proj", w.PATH_GEMV), (3, "gate_up", w.PATH_TC), (4, "down", w.PATH_TC),
-                           (8, "qkv", w.PATH_TC), (16, "qkv", w.PATH_TC), (1, "vocab", w.PATH_GEMV),
-                           (4, "vocab", w.PATH_TC)]:
+    rows, limits = _dispatch_rows()
+    assert rows
+    for shape in list(wi.LAYER) + ["vocab"]:
         K, N = wi.shape_kn(shape)
-        assert w.w4a16_auto_path(M, N, K) == want, (M, shape)
+        cls = sum(K * N > v for v in limits)
+        mine = [r for r in rows if r[0] == cls]
+        for M in (1, 2, 3, 4, 5, 8, 9, 16, 20, 33, 64, 100, 128, 300, 2048, 8192, 9000):
+            row = next((r for r in mine if M <= r[1]), mine[-1])
+            want = row[2] if M <= 8 or row[2] == TC else TC
+            assert w.w4a16_auto_path(M, N, K) == want, (shape, M, row)
