@@ -316,9 +316,12 @@ int w4a16_gemm_noalloc(const void *x, const uint32_t *qweight_dev, const void *s
  *   head_dim   128 (W4A16_EUNSUPPORTED otherwise); Hq % Hkv == 0;
  *              nq * Hq / Hkv <= 128 (W4A16_EUNSUPPORTED); 1 <= nq <= L <= Lmax;
  *              Lmax % 8 == 0; window >= 1; block 0 or 1 (W4A16_EINVAL)
- *   workspace  caller-owned, zero-filled once, w4a16_swa_workspace_bytes bytes
- *              (W4A16_EWORKSPACE if missing or short); each call leaves its
- *              counters at zero again
+ *   workspace  caller-owned scratch of w4a16_swa_workspace_bytes bytes for the
+ *              f32 partial results of the key chunks (W4A16_EWORKSPACE if
+ *              missing or short); its first 64 KB are never written, so the
+ *              same buffer may also be a GEMM workspace (whose arrival
+ *              counters live there).  Two launches: the chunks, then their
+ *              combine.
  *   flags      0 or W4A16_FLAG_PDL
  *
  * All pointers 16-byte aligned (W4A16_EALIGN); out may not overlap the

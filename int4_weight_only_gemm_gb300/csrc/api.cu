@@ -435,7 +435,7 @@ int w4a16_swa_attention(const void* q, const void* k_cache, const void* vt_cache
                    block, workspace, sp, reinterpret_cast<cudaStream_t>(stream), (flags & W4A16_FLAG_PDL) != 0) !=
         cudaSuccess)
         return W4A16_ECUDA;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
+    g_launches.fetch_add(2, std::memory_order_relaxed);  // the chunk kernel and the combine
     return W4A16_OK;
 }
 

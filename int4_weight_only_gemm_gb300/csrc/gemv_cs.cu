@@ -11,30 +11,31 @@
 // that a gate column and its up column stay together), so no CTA ever hands
 // a partial sum to another and no workspace is needed.  Inside the CTA,
 // thread t takes column j = t % C of the slice and the range s = t / C of
-// the K split (S = 512 / C ranges), or, for slices wider than half the
-// block, whole columns j = t, t + 512, ...
+// whole 128-row groups of K (S = min(512 / C, K / 128) ranges), or, for
+// slices wider than half the block, whole columns j = t, t + 512, ...
 //
 // Data movement: the unit of work is an item, one column's 32 rows of K: 16
 // bytes of the device layout (word j of chunk c holds rows 8(4c + j)..+7).
 // A column's items lie a constant W * 16 bytes apart (W = width of its
 // 128-column tile), and the lanes of a warp read adjacent columns, so each
-// load instruction of a warp fetches contiguous runs.  Each thread keeps D
-// items in flight in a register ring (16-byte global loads, no L1
-// allocation): no shared-memory staging of weights at all.
+// copy instruction of a warp fetches contiguous runs.  Each thread streams
+// its items with 16-byte asynchronous copies into a private ring of D + 1
+// shared-memory slots, D items ahead of the one it multiplies: the distance
+// is fixed by the copies in flight, not by register scheduling.
 //
-// Arithmetic: per item and token, dot = sum over the 32 rows of (128 + q) x
-// with the bfloat16 value 128 + q made by one mask-and-or per pair of rows
-// (exact) and bf16 x bf16 -> f32 fused multiply-adds; the zero point and
-// scale then apply once per item in f32: acc += s (dot - (128 + z) xs), xs =
-// the sum of the item's 32 activations (computed once per CTA).  The scale
-// is used at its full binary16 precision.  The K ranges of a column are
-// added through shared memory in range order: the result does not depend on
-// timing.
+// Arithmetic: per item and token, the dot product of the 32 rows with x,
+// sum (128 + q) x, with the bfloat16 value 128 + q made by one mask-and-or
+// per pair of rows (exact) and bf16 x bf16 -> f32 fused multiply-adds in
+// four independent chains; the zero point and scale apply once per 128-row
+// group in f32: acc += s (dot - (128 + z) xs), xs = the group's sum of x
+// (computed once per CTA).  The scale is used at its full binary16 precision.
+// The K ranges of a column are added through shared memory in range order:
+// the result does not depend on timing.
 //
-// Footprint: at M <= 2 a CTA uses at most 64 registers a thread and about
-// 30 KB of shared memory for the decoder's shapes, so two CTAs fit on an SM:
-// the next programmatic-dependent GEMM of a chain becomes resident while this
-// one runs, and with static weights starts its loads before the grid
+// Footprint: at M <= 2 a CTA takes at most 64 registers a thread and, for the
+// decoder's shapes, at most ~100 KB of shared memory, so two CTAs fit on an
+// SM: the next programmatic-dependent GEMM of a chain becomes resident while
+// this one runs, and with static weights starts its copies before the grid
 // dependency resolves.
 #include "common.cuh"
 #include "kernels.h"
@@ -47,10 +48,10 @@ struct CsParams {
     const uint16_t* scales;
     const uint32_t* qzeros;
     uint16_t* y;
-    int M, N, K, R, KB;  // R = K / 32 items per column
-    int U, unit;         // column units and their width (4, or 16 for fused gate/up)
-    int prefetch;        // weights, scales and zeros may be read before the preceding grid completes
-    int guH;             // > 0: fused gate/up weights (N = 2 guH); y[M][guH] = silu(gate) * up
+    int M, N, K, KB;  // KB = K / 128 groups
+    int U, unit;      // column units and their width (4, or 16 for fused gate/up)
+    int prefetch;     // weights, scales and zeros may be read before the preceding grid completes
+    int guH;          // > 0: fused gate/up weights (N = 2 guH); y[M][guH] = silu(gate) * up
 };
 
 constexpr int kCsThreads = 512;
@@ -58,33 +59,26 @@ constexpr int kCsThreads = 512;
 // Shared-memory layout (bytes from the dynamic base), identical on both
 // sides; every region starts on a 16-byte boundary.
 struct CsSmem {
-    size_t xs, xsum, sc, zr, red, total;
+    size_t xs, xsum, sc, zr, ring, red, total;
     static __host__ __device__ size_t up16(size_t v) { return (v + 15) & ~(size_t)15; }
-    // MT: token rows held (M rounded up), C: slice width.  Every region grows
-    // with C, so the widest slice of a launch sizes it for all its CTAs.
-    __host__ __device__ CsSmem(int MT, int K, int C) {
-        const int R = K / 32, G = K / 128;
+    // MT: token rows held (M rounded up), C: slice width, D: items in flight a
+    // thread.  Every region grows with C, so the widest slice of a launch sizes
+    // it for all its CTAs.
+    __host__ __device__ CsSmem(int MT, int K, int C, int D) {
+        const int G = K / 128;
         xs = 0;                                          // [MT][K] bf16 activations
-        xsum = up16(xs + (size_t)MT * K * 2);            // [MT][R] f32 item sums of x
-        sc = up16(xsum + (size_t)MT * R * 4);            // [G][C] fp16 scales of the slice
+        xsum = up16(xs + (size_t)MT * K * 2);            // [MT][G] f32 group sums of x
+        sc = up16(xsum + (size_t)MT * G * 4);            // [G][C] fp16 scales of the slice
         zr = up16(sc + (size_t)G * C * 2);               // [G][C/4] zero words, one per run of 4 columns
-        red = up16(zr + (size_t)G * C);                  // [S][C][MT] f32 partial sums (S C <= max(512, C))
+        ring = up16(zr + (size_t)G * C);                 // [D + 1][512] 16-byte item slots
+        red = ring + (size_t)(D + 1) * kCsThreads * 16;  // [S][C][MT] f32 partial sums (S C <= max(512, C))
         total = up16(red + (size_t)(C > kCsThreads ? C : kCsThreads) * MT * 4);
     }
 };
 
-__host__ __device__ inline int cs_ranges(int C, int R) {
+__host__ __device__ inline int cs_ranges(int C, int G) {
     int S = C >= kCsThreads / 2 ? 1 : kCsThreads / C;
-    return S < R ? S : R;
-}
-
-// 16-byte load that bypasses L1 (weights are read once).
-W4A16_DEVICE uint4 ldg_stream(const uint4* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
+    return S < G ? S : G;
 }
 
 template <int MT, int D>
@@ -96,46 +90,55 @@ __global__ void __launch_bounds__(kCsThreads, MT <= 2 ? 2 : 1) gemv_cs_kernel(co
     const int c0 = p.unit * (int)((long long)b * p.U / P);
     const int c1 = p.unit * (int)((long long)(b + 1) * p.U / P);
     const int C = c1 - c0;
-    const int R = p.R, G = p.KB;
-    const int S = cs_ranges(C, R);
-    const CsSmem lay(MT, p.K, C);
+    const int G = p.KB;
+    const int S = cs_ranges(C, G);
+    const CsSmem lay(MT, p.K, C, D);
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + lay.xs);
     float* xsum = reinterpret_cast<float*>(smem + lay.xsum);
     uint16_t* ssc = reinterpret_cast<uint16_t*>(smem + lay.sc);
     uint32_t* szw = reinterpret_cast<uint32_t*>(smem + lay.zr);
+    uint4* ring = reinterpret_cast<uint4*>(smem + lay.ring) + t;  // slot k of this thread at ring[k * 512]
     float* red = reinterpret_cast<float*>(smem + lay.red);
 
     // the next grid in the stream may start as soon as every CTA of this one runs
     pdl_launch_dependents();
 
-    // this thread's work: column j (then j + 512, ... when S == 1) over items [r0, r1)
+    // this thread's work: column j0 (then j0 + 512, ... when S == 1), groups [g0, g1)
     const bool active = t < S * C || S == 1;
     const int j0 = S == 1 ? t : t % C;
     const int s = S == 1 ? 0 : t / C;
-    const int r0 = (int)((long long)s * R / S), r1 = (int)((long long)(s + 1) * R / S);
-    const int nr = r1 - r0;
+    const int g0 = (int)((long long)s * G / S), g1 = (int)((long long)(s + 1) * G / S);
+    const int nr = 4 * (g1 - g0);  // items of one column
     const int npass = S == 1 ? (j0 < C ? (C - j0 + kCsThreads - 1) / kCsThreads : 0) : (active ? 1 : 0);
     const int nitems = npass * nr;
     const uint4* qd4 = reinterpret_cast<const uint4*>(p.qd);
 
-    // item address: column n, item r -> uint4 index 512 KB nb + W r + (n % 128);
-    // a column's items are W uint4 apart
-    const uint4* cptr = nullptr;
-    size_t cstride = 0;
-    uint4 ring[D];
-    // the first D items of pass `pass` (column j0 + 512 pass) into the ring
-    auto start_column = [&](int pass) {
+    // Copy cursor over this thread's items, pass by pass: item r of column n
+    // is uint4 512 KB nb + W r + (n % 128) of the device layout (W = width of
+    // tile nb), so a column's items are W uint4 apart.
+    const uint4* lptr = nullptr;
+    int lstride = 0, lp = 0, lr = 0, issued = 0;
+    auto set_column = [&](int pass) {
         const int n = c0 + j0 + pass * kCsThreads;
         const int nb = n >> 7;
-        cstride = (size_t)(p.N - 128 * nb < 128 ? p.N - 128 * nb : 128);
-        cptr = qd4 + (size_t)512 * p.KB * nb + cstride * r0 + (n & 127);
-#pragma unroll
-        for (int i = 0; i < D; ++i)
-            if (i < nr) ring[i] = ldg_stream(cptr + i * cstride);
+        lstride = p.N - 128 * nb < 128 ? p.N - 128 * nb : 128;
+        lptr = qd4 + (size_t)512 * p.KB * nb + (size_t)lstride * (4 * g0) + (n & 127);
+    };
+    // item `issued` into its slot, one commit group per item (possibly empty)
+    auto copy_next = [&]() {
+        if (issued < nitems) {
+            cp_async_16(ring + (size_t)(issued % (D + 1)) * kCsThreads, lptr);
+            lptr += lstride;
+            if (++lr == nr) {
+                lr = 0;
+                if (++lp < npass) set_column(lp);
+            }
+            ++issued;
+        }
+        cp_async_commit();
     };
     // The slice's scales ([G][C] fp16, device-column order) and, per run of
-    // four columns, the zero word holding their zero points ([G][C/4]), as
-    // asynchronous copies: every copy of the CTA is in flight at once.  Four
+    // four columns, the zero word holding their zero points ([G][C/4]).  Four
     // adjacent device columns are four adjacent canonical columns in both
     // layouts, and a column's zero nibble sits at bit 4 (n % 8) of its word.
     auto stage_scales_zeros = [&]() {
@@ -147,15 +150,21 @@ __global__ void __launch_bounds__(kCsThreads, MT <= 2 ? 2 : 1) gemv_cs_kernel(co
             cp_async_8(ssc + (size_t)g * C + jj, p.scales + (size_t)g * p.N + cn);
             cp_async_4(szw + i, p.qzeros + (size_t)g * (p.N / 8) + (cn >> 3));
         }
+        cp_async_commit();
+    };
+    auto start_items = [&]() {
+        if (nitems > 0) set_column(0);
+#pragma unroll 1
+        for (int i = 0; i < D; ++i) copy_next();
     };
 
     if (p.prefetch) {
-        if (npass > 0) start_column(0);
+        start_items();
         stage_scales_zeros();
     }
     pdl_wait();  // x, and y below, only after the preceding grid
     if (!p.prefetch) {
-        if (npass > 0) start_column(0);
+        start_items();
         stage_scales_zeros();
     }
     {
@@ -169,74 +178,83 @@ __global__ void __launch_bounds__(kCsThreads, MT <= 2 ? 2 : 1) gemv_cs_kernel(co
             else xv[i] = make_uint4(0, 0, 0, 0);
         }
         cp_async_commit();
-        cp_async_wait<0>();
+        cp_async_wait<0>();  // the first D items, the scales and zeros, and x
     }
     __syncthreads();
-    // per-item activation sums, one (token, item) per thread
-    for (int i = t; i < MT * R; i += kCsThreads) {
-        const uint4* xr = reinterpret_cast<const uint4*>(xs) + (size_t)i * 4;
-        float a = 0.f;
+    // per-group activation sums, one (token, group) per warp
+    {
+        const int warp = t >> 5, lane = t & 31;
+        for (int i = warp; i < MT * G; i += kCsThreads / 32) {
+            const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs) + (size_t)i * 64;
+            const uint32_t v0 = xr[lane], v1 = xr[lane + 32];
+            float a = (bf16lo(v0) + bf16hi(v0)) + (bf16lo(v1) + bf16hi(v1));
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 v = xr[q];
-            a += (bf16lo(v.x) + bf16hi(v.x)) + (bf16lo(v.y) + bf16hi(v.y)) + (bf16lo(v.z) + bf16hi(v.z)) +
-                 (bf16lo(v.w) + bf16hi(v.w));
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+            if (lane == 0) xsum[i] = a;
         }
-        xsum[i] = a;
     }
     __syncthreads();
 
     const uint32_t xs_a = smem_u32(xs);
+    const uint32_t ring_a = smem_u32(ring);
     const uint32_t xrow = (uint32_t)p.K * 2;  // bytes between token rows of xs
+    constexpr int NCH = MT == 1 ? 4 : 2;      // independent chains a token
+    int k = 0;                                // item being multiplied
+#pragma unroll 1
     for (int pass = 0; pass < npass; ++pass) {
-        if (pass > 0) start_column(pass);
         const int jj = j0 + pass * kCsThreads;
         const uint32_t zsh = 4u * (uint32_t)((c0 + jj) & 7);  // this column's nibble in its zero word
         float acc[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-        // D items per round, so the ring is indexed with constants
-        for (int base = 0; base < nr; base += D) {
+#pragma unroll 1
+        for (int g = g0; g < g1; ++g) {
+            float d[MT][NCH];
 #pragma unroll
-            for (int u = 0; u < D; ++u) {
-                const int i = base + u;
-                if (i < nr) {
-                    const uint32_t wv[4] = {ring[u].x, ring[u].y, ring[u].z, ring[u].w};
-                    if (i + D < nr) ring[u] = ldg_stream(cptr + (size_t)(i + D) * cstride);
-                    const int r = r0 + i;
-                    const int g = r >> 2;
-                    const float sc = f16_bits_to_f32(ssc[g * C + jj]);
-                    const float zoff = 128.f + (float)((szw[g * (C >> 2) + (jj >> 2)] >> zsh) & 0xFu);
-                    float d[MT][2];
+            for (int m = 0; m < MT; ++m)
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) d[m][0] = d[m][1] = 0.f;
+                for (int c = 0; c < NCH; ++c) d[m][c] = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {  // word q: rows 8q .. 8q + 7 of the item
+            for (int it = 0; it < 4; ++it, ++k) {  // the group's four items
+                cp_async_wait<D - 1>();            // item k has landed (D - 1 newer copies may be pending)
+                const uint4 w = lds_v4(ring_a + (uint32_t)(k % (D + 1)) * (kCsThreads * 16));
+                copy_next();                       // item k + D, into the slot item k - 1 used
+                const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                const int r = 4 * g + it;
 #pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            const uint4 xq = lds_v4(xs_a + (uint32_t)m * xrow + (uint32_t)r * 64 + (uint32_t)q * 16);
-                            const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
-                            float a = d[m][q & 1];
+                for (int q = 0; q < 4; ++q) {  // word q: rows 8q .. 8q + 7 of the item
 #pragma unroll
-                            for (int pp = 0; pp < 4; ++pp) {
-                                const uint32_t wp = magic_pair(wv[q], pp);
-                                a = fma_lo(wp, xp[pp], a);
-                                a = fma_hi(wp, xp[pp], a);
-                            }
-                            d[m][q & 1] = a;
+                    for (int m = 0; m < MT; ++m) {
+                        const uint4 xq = lds_v4(xs_a + (uint32_t)m * xrow + (uint32_t)r * 64 + (uint32_t)q * 16);
+                        const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
+                        float a = d[m][q % NCH];
+#pragma unroll
+                        for (int pp = 0; pp < 4; ++pp) {
+                            const uint32_t wp = magic_pair(wv[q], pp);
+                            a = fma_lo(wp, xp[pp], a);
+                            a = fma_hi(wp, xp[pp], a);
                         }
+                        d[m][q % NCH] = a;
                     }
-#pragma unroll
-                    for (int m = 0; m < MT; ++m)
-                        acc[m] = fmaf(sc, fmaf(-zoff, xsum[m * R + r], d[m][0] + d[m][1]), acc[m]);
                 }
+            }
+            const float sc = f16_bits_to_f32(ssc[g * C + jj]);
+            const float zoff = 128.f + (float)((szw[g * (C >> 2) + (jj >> 2)] >> zsh) & 0xFu);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                float dot = d[m][0];
+#pragma unroll
+                for (int c = 1; c < NCH; ++c) dot += d[m][c];
+                acc[m] = fmaf(sc, fmaf(-zoff, xsum[m * G + g], dot), acc[m]);
             }
         }
         // this column's sums over this thread's K range
 #pragma unroll
         for (int m = 0; m < MT; ++m) red[((size_t)s * C + jj) * MT + m] = acc[m];
     }
+    cp_async_wait<0>();  // the trailing commit groups are empty; nothing stays in flight
     __syncthreads();
+
     // the K ranges of each column added in range order; fused weights: the
     // gate column (device column d, d % 16 < 8) meets its up column d + 8
     for (int i = t; i < C * MT; i += kCsThreads) {
@@ -266,6 +284,7 @@ __global__ void __launch_bounds__(kCsThreads, MT <= 2 ? 2 : 1) gemv_cs_kernel(co
 static int cs_mtile(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
 constexpr int kCsMaxSmem = 226 * 1024;
 
+// Items in flight a thread: 8, or 4 where 8 would not fit the shared memory.
 bool gemv_cs_plan(int M, int N, int K, int sms, int guH, GemvCsPlan* out) {
     if (M < 1 || M > 8 || sms < 1 || K < 128 || K % 128 || N % 8) return false;
     const int unit = guH ? 16 : 4;
@@ -275,11 +294,14 @@ bool gemv_cs_plan(int M, int N, int K, int sms, int guH, GemvCsPlan* out) {
     const int MT = cs_mtile(M);
     // the widest slice decides the shared memory
     const int C = (int)(unit * ((U + P - 1) / P));
-    const CsSmem lay(MT, K, C);
+    int D = 8;
+    if (CsSmem(MT, K, C, D).total > (size_t)kCsMaxSmem) D = 4;
+    const CsSmem lay(MT, K, C, D);
     if (lay.total > (size_t)kCsMaxSmem) return false;
     out->ctas = P;
     out->U = (int)U;
     out->unit = unit;
+    out->D = D;
     out->smem = lay.total;
     return true;
 }
@@ -312,18 +334,18 @@ cudaError_t launch_gemv_cs(const uint16_t* x, const uint32_t* qd, const uint16_t
     prm.M = M;
     prm.N = N;
     prm.K = K;
-    prm.R = K / 32;
     prm.KB = K / 128;
     prm.U = plan.U;
     prm.unit = plan.unit;
     const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     prm.guH = guH;
+    const bool deep = plan.D == 8;
     switch (cs_mtile(M)) {
-        case 1: return launch_cs<1, 8>(prm, plan, s, pdl);
-        case 2: return launch_cs<2, 4>(prm, plan, s, pdl);
-        case 4: return launch_cs<4, 4>(prm, plan, s, pdl);
-        default: return launch_cs<8, 4>(prm, plan, s, pdl);
+        case 1: return deep ? launch_cs<1, 8>(prm, plan, s, pdl) : launch_cs<1, 4>(prm, plan, s, pdl);
+        case 2: return deep ? launch_cs<2, 8>(prm, plan, s, pdl) : launch_cs<2, 4>(prm, plan, s, pdl);
+        case 4: return deep ? launch_cs<4, 8>(prm, plan, s, pdl) : launch_cs<4, 4>(prm, plan, s, pdl);
+        default: return deep ? launch_cs<8, 8>(prm, plan, s, pdl) : launch_cs<8, 4>(prm, plan, s, pdl);
     }
 }
 

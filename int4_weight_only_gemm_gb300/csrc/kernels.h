@@ -63,6 +63,7 @@ int gemv_read_status();
 struct GemvCsPlan {
     int ctas;        // one per SM (fewer when the columns are fewer)
     int U, unit;     // column units and their width
+    int D;           // items in flight a thread (8 or 4)
     size_t smem;
 };
 bool gemv_cs_plan(int M, int N, int K, int sms, int guH, GemvCsPlan* out);
@@ -108,7 +109,7 @@ int tc_read_status();
 struct SwaPlan {
     int j0, C;       // first key (a multiple of 8) and 128-key chunks of the block's window
     int G, R;        // query heads per key / value head; query rows per head group (nq G)
-    size_t ws_bytes;  // the arrival counters, then the f32 partials
+    size_t ws_bytes;  // the f32 partials
 };
 bool swa_plan(int nq, int Hq, int Hkv, int L, int W, int block, SwaPlan* out);
 cudaError_t launch_swa(const uint16_t* q, const uint16_t* kc, const uint16_t* vtc, uint16_t* out, int nq, int Hq,

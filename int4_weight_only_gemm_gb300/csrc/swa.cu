@@ -27,9 +27,10 @@
 //   * warp 4 issues the 8 MMAs of O = P V (A = P from TMEM, B = the value
 //     chunk), and the row threads store O, m and l of their row as f32
 //     partials;
-//   * the last CTA of a head to finish (arrival counter) combines the chunks
-//     of every row, out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c, and
-//     writes bfloat16; the partials of a call stay in L2.
+//   * a second kernel (a programmatic dependent) combines the chunks of every
+//     row, out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c, one CTA per
+//     query and head group, and writes bfloat16; the partials of a call stay
+//     in L2.
 //
 // Every wait is bounded (common.cuh); on a timeout the kernel records
 // W4A16_ETIMEOUT, still drains its tensor-core work, frees its tensor memory
@@ -47,7 +48,6 @@ static __device__ int g_swa_status;
 struct SwaParams {
     const uint16_t* q;   // [nq][Hq][128] bf16
     uint16_t* out;       // [nq][Hq][128] bf16
-    uint32_t* counters;  // [Hkv]
     float* part_o;       // [Hkv][C][128][128]
     float* part_ml;      // [Hkv][C][128][2]
     int nq, Hq, Hkv, G, R, L, W, block, j0, C;
@@ -95,7 +95,6 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
     uint64_t* o_bar = bars + 4;    // O = P V done
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    int* sh_last = const_cast<int*>(abort_flag) + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x, hk = blockIdx.y;
@@ -261,45 +260,37 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
         if (!ok) *abort_flag = 1;
     }
 
-    // ---- the last CTA of this head combines the chunks
-    tc_fence_before();
-    __syncthreads();
-    const bool all_ok = !*abort_flag;
-    if (threadIdx.x == 0) {
-        int last = 0;
-        if (all_ok) {
-            __threadfence();
-            const unsigned old = atomicAdd(&p.counters[hk], 1u);
-            last = old == (unsigned)p.C - 1;
-            if (last) __threadfence();
-        }
-        *sh_last = last;
-    }
-    __syncthreads();
-    if (*sh_last && threadIdx.x < kSwaD) {
-        const int t = threadIdx.x;  // column of the head
-        for (int r = 0; r < p.R; ++r) {
-            float M = -INFINITY;
-            for (int cc = 0; cc < p.C; ++cc) M = fmaxf(M, __ldcg(p.part_ml + (((size_t)hk * p.C + cc) * 128 + r) * 2));
-            float num = 0.f, den = 0.f;
-            for (int cc = 0; cc < p.C; ++cc) {
-                const size_t row = ((size_t)hk * p.C + cc) * 128 + r;
-                const float mc = __ldcg(p.part_ml + row * 2);
-                if (mc == -INFINITY) continue;  // no key of this row's window in chunk cc
-                const float f = exp2f(mc - M);
-                num = fmaf(f, __ldcg(p.part_o + row * kSwaD + t), num);
-                den = fmaf(f, __ldcg(p.part_ml + row * 2 + 1), den);
-            }
-            const int qi = r / p.G, hh = r - (r / p.G) * p.G;
-            p.out[((size_t)qi * p.Hq + (size_t)hk * p.G + hh) * kSwaD + t] = f32_to_bf16_rn(num / den);
-        }
-        if (t == 0) p.counters[hk] = 0u;
-    }
     tc_fence_before();
     __syncthreads();
     if (warp == 4) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+}
+
+// Combine the chunks of the query rows of one (query, key/value head): CTA
+// (qi, hk), thread t = column t of the head, for each of the G heads of the
+// group: M = max_c m_c, out = sum_c 2^(m_c - M) O_c[t] / sum_c 2^(m_c - M) l_c.
+// Branch-free so that the loads of all chunks are in flight together.
+__global__ void __launch_bounds__(kSwaD) swa_combine_kernel(const SwaParams p) {
+    pdl_wait();  // the partials of the chunk kernel
+    const int qi = blockIdx.x, hk = blockIdx.y, t = threadIdx.x;
+    for (int hh = 0; hh < p.G; ++hh) {
+        const int r = qi * p.G + hh;
+        float M = -INFINITY;
+        for (int c = 0; c < p.C; ++c) M = fmaxf(M, __ldcg(p.part_ml + (((size_t)hk * p.C + c) * 128 + r) * 2));
+        float num = 0.f, den = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < p.C; ++c) {
+            const size_t row = ((size_t)hk * p.C + c) * 128 + r;
+            const float mc = __ldcg(p.part_ml + row * 2);
+            const float lc = __ldcg(p.part_ml + row * 2 + 1);
+            const float oc = __ldcg(p.part_o + row * kSwaD + t);
+            const float f = mc == -INFINITY ? 0.f : exp2f(mc - M);  // no key of this row's window in chunk c
+            num = fmaf(f, oc, num);
+            den = fmaf(f, lc, den);
+        }
+        p.out[((size_t)qi * p.Hq + (size_t)hk * p.G + hh) * kSwaD + t] = f32_to_bf16_rn(num / den);
     }
 }
 
@@ -322,9 +313,11 @@ static PFN_cuTensorMapEncodeTiled_v12000 swa_encode() {
     return fn;
 }
 
-// workspace: one arrival counter per key / value head (a whole number of
-// 256-byte blocks), then the f32 partials
-static size_t swa_counter_bytes(int Hkv) { return ((size_t)Hkv * 4 + 255) / 256 * 256; }
+// Workspace: the f32 partials (m and l of every row and chunk, then O) after
+// the 64 KB area where the GEMM kernels keep their split-K arrival counters.
+// That area is never written here, so one buffer can serve both calls: the
+// counters must stay zero between GEMM calls.
+static size_t swa_counter_bytes(int) { return kCounterBytes; }
 
 bool swa_plan(int nq, int Hq, int Hkv, int L, int W, int block, SwaPlan* out) {
     const int e0 = block ? L - 1 : L - nq;  // the first query's last visible key
@@ -371,7 +364,6 @@ cudaError_t launch_swa(const uint16_t* q, const uint16_t* kc, const uint16_t* vt
     SwaParams prm;
     prm.q = q;
     prm.out = out;
-    prm.counters = reinterpret_cast<uint32_t*>(ws);
     prm.part_ml = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + swa_counter_bytes(Hkv));
     prm.part_o = prm.part_ml + (size_t)Hkv * plan.C * 128 * 2;
     prm.nq = nq;
@@ -394,7 +386,9 @@ cudaError_t launch_swa(const uint16_t* q, const uint16_t* kc, const uint16_t* vt
         if (e != cudaSuccess) return e;
         set_for[dev] = 1;
     }
-    return launch_kernel(swa_kernel, dim3(plan.C, Hkv), dim3(kSwaThreads), (size_t)kSwaSmem, s, pdl, tk, tv, prm);
+    e = launch_kernel(swa_kernel, dim3(plan.C, Hkv), dim3(kSwaThreads), (size_t)kSwaSmem, s, pdl, tk, tv, prm);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(swa_combine_kernel, dim3(nq, Hkv), dim3(kSwaD), 0, s, true, prm);
 }
 
 int swa_read_status() {

@@ -86,7 +86,9 @@ def test_swa_deterministic_and_workspace_reused():
     a = run(q, k, v, 3000, 2048, False, ws)
     b = run(q, k, v, 3000, 2048, False, ws)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-    assert ws.view(torch.int32)[:8].abs().sum().item() == 0  # counters back at zero
+    n0 = w.w4a16_launch_count()
+    run(q, k, v, 3000, 2048, False, ws)
+    assert w.w4a16_launch_count() == n0 + 2  # the chunk kernel and the combine
     assert w.w4a16_last_device_status() == 0
 
 
@@ -122,3 +124,23 @@ def test_swa_argument_errors():
     assert call(wsb=16) == w.W4A16_EWORKSPACE
     torch.cuda.synchronize()
     assert w.w4a16_last_device_status() == 0
+
+
+def test_swa_shares_a_workspace_with_the_gemm():
+    """One buffer as the workspace of the attention and of a split-K GEMM: the
+    attention leaves the GEMM's arrival counters (the first 64 KB) at zero."""
+    import int4_weight_only_gemm_gb300 as w
+    import oracle
+    from tests.gpu_helpers import Device, bf16_to_f64, check_close
+    p = wi.generate_named("qkv", 1, 60)
+    d = Device(p)
+    q, k, v = make(16, 32, 8, 2304, 2304, seed=61)
+    need = max(w.w4a16_workspace_bytes(1, p.N, p.K, path=w.PATH_GEMV_SPLITK),
+               w.w4a16_swa_workspace_bytes(16, 32, 8, 2304, 1024))
+    ws = w.new_workspace(need)
+    for _ in range(2):
+        run(q, k, v, 2304, 1024, False, ws)
+        assert ws[:65536].view(torch.int32).abs().sum().item() == 0
+        y = d.run(w.PATH_GEMV_SPLITK, workspace=ws)
+        torch.cuda.synchronize()
+        check_close(bf16_to_f64(y), oracle.gemm(p.x, p.qweight, p.scales, p.qzeros), "split-K after attention")
