@@ -67,9 +67,9 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-# The sources the GEMV kernel and its planner are compiled from: a traffic
-# figure measured by ncu stays valid while these are unchanged.
-GEMV_SOURCES = ("common.cuh", "gemv.cu")
+# The sources a kernel is compiled from: a traffic figure measured by ncu stays
+# valid while these are unchanged (each entry of profiles/traffic.json names them).
+GEMV_SOURCES = ("common.cuh", "gemv.cu", "gemv_cs.cu")
 
 
 def kernel_source_sha(names=GEMV_SOURCES):
@@ -81,9 +81,9 @@ def kernel_source_sha(names=GEMV_SOURCES):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_key):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel sources
-    still match the ones profiled; else None."""
+def profiled_traffic(kernel_key, field="dram_bytes_per_step"):
+    """DRAM bytes from a committed ncu summary, if the kernel sources still
+    match the ones profiled; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -91,9 +91,9 @@ def profiled_traffic(kernel_key):
     except Exception:
         return None
     e = d.get(kernel_key)
-    if not e or e.get("source_sha") != kernel_source_sha():
+    if not e or e.get("source_sha") != kernel_source_sha(tuple(e.get("sources", GEMV_SOURCES))):
         return None
-    return e.get("dram_bytes_per_step")
+    return e.get(field)
 
 
 class ClockSampler:
@@ -237,7 +237,7 @@ class Workload:
             qds = [qd] + [qd.clone() for _ in range(copies - 1)]
             del qw
             y = torch.empty((M, p.N), dtype=torch.bfloat16, device=device)
-            need = w.w4a16_workspace_bytes(M, p.N, p.K)
+            need = w.w4a16_workspace_bytes_max(M, p.N, p.K)  # any path or token tile
             ws = w.new_workspace(need, device)
             self.gemms.append(dict(p=p, shape=shape, M=M, K=p.K, N=p.N, x=x, qds=qds, sc=sc, qz=qz, y=y, ws=ws,
                                    ws_bytes=ws.numel()))
@@ -245,7 +245,7 @@ class Workload:
         self.bytes = sum(gemm_bytes(g["M"], g["K"], g["N"]) for g in self.gemms)
         self.flops = sum(gemm_flops(g["M"], g["K"], g["N"]) for g in self.gemms)
 
-    def launch_step(self, copy, stream_ptr, only=None, flags=None):
+    def launch_step(self, copy, stream_ptr, only=None, flags=None, path=0):
         w = self.w
         n = 0
         for i, g in enumerate(self.gemms):
@@ -253,32 +253,32 @@ class Workload:
                 continue
             st = w.w4a16_gemm_raw(g["x"].data_ptr(), g["qds"][copy].data_ptr(), g["sc"].data_ptr(),
                                   g["qz"].data_ptr(), g["M"], g["N"], g["K"], 128, g["y"].data_ptr(),
-                                  g["ws"].data_ptr(), g["ws_bytes"], 0, stream_ptr, flags)
+                                  g["ws"].data_ptr(), g["ws_bytes"], path, stream_ptr, flags)
             if st != 0:
                 raise RuntimeError(f"w4a16_gemm failed: {w.w4a16_status_str(st)}")
             n += 1
         return n
 
-    def graphs(self, only=None, flags=None):
+    def graphs(self, only=None, flags=None, path=0):
         """One graph per weight copy (a step each) and one for the whole rotation."""
         torch = self.torch
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
             for c in range(self.copies):  # warm-up outside capture
-                self.launch_step(c, s.cuda_stream, only, flags)
+                self.launch_step(c, s.cuda_stream, only, flags, path)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         per_step = []
         for c in range(self.copies):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                self.launch_step(c, torch.cuda.current_stream().cuda_stream, only, flags)
+                self.launch_step(c, torch.cuda.current_stream().cuda_stream, only, flags, path)
             per_step.append(g)
         rot = torch.cuda.CUDAGraph()
         with torch.cuda.graph(rot):
             for c in range(self.copies):
-                self.launch_step(c, torch.cuda.current_stream().cuda_stream, only, flags)
+                self.launch_step(c, torch.cuda.current_stream().cuda_stream, only, flags, path)
         torch.cuda.synchronize()
         return per_step, rot
 
@@ -715,6 +715,7 @@ def main():
                          "PATH 0 = auto, 1 = split-K GEMV, 2 = tensor-core kernel")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--no-sweep", action="store_true", help="skip the M sweep")
+    ap.add_argument("--only", default="", help="comma-separated extras to run (default: all)")
     ap.add_argument("--tune-dispatch", default="",
                     help="OUT.json -- time every dispatch candidate over the sweep, write them and exit")
     ap.add_argument("--tune-m", default="", help="comma-separated M values for --tune-dispatch (default: all)")
@@ -779,14 +780,17 @@ def main():
     failed = []  # extras that raised: the error goes into the line, later GPU extras are skipped
 
     def guarded(name, fn):
+        if args.only and name not in args.only.split(","):
+            return
         if failed:
             extra[name] = {"skipped": f"after the failure of {failed[0]}"}
             return
         try:
             fn()
-        except Exception as exc:  # a CUDA error leaves the context unusable: stop all GPU work
-            failed.append(name)
+        except Exception as exc:
             extra[name] = {"error": repr(exc)[:400]}
+            if "CUDA" in repr(exc) or "cuda" in type(exc).__name__.lower() or "Accelerator" in type(exc).__name__:
+                failed.append(name)  # the context is unusable: no more GPU work
 
     def ex_decode_per_gemm():
         # each projection alone (graph of the 8-copy rotation of that GEMM)
@@ -803,11 +807,14 @@ def main():
     def ex_decode_flags():
         # the decode set under each launch-flag combination
         fl = {}
-        for flags, name in ((0, "plain"), (1, "pdl"), (3, "pdl_static_weights")):
-            ps, rt = wl.graphs(flags=flags)
+        for flags, name, path in ((0, "plain", 0), (1, "pdl", 0), (3, "pdl_static_weights", 0),
+                                  (1, "pdl_all_column_sliced", 4), (3, "pdl_static_all_column_sliced", 4),
+                                  (3, "pdl_static_all_split_k", 3)):
+            ps, rt = wl.graphs(flags=flags, path=path)
             n = max(200, min(args.steps, 20000))
             t_ms = time_graph_steps(torch, ps, rt, COPIES, n, 50)
-            fl[name] = {"us_per_step": t_ms / n * 1e3, "GB/s": wl.bytes * n / (t_ms / 1e3) / 1e9}
+            fl[name] = {"us_per_step": t_ms / n * 1e3, "GB/s": wl.bytes * n / (t_ms / 1e3) / 1e9,
+                        "path": PATH_NAMES.get(path, "auto")}
         extra["decode_m1_flags"] = fl
 
     def ex_workload(name, unit):
@@ -894,13 +901,32 @@ def main():
                        "bytes_per_step": wl.bytes, "launch": "CUDA graph of the 8-copy rotation"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": traffic,
-                         "kernel": "gemv_kernel<1> (all four GEMMs of the step)",
+                         "kernel": "the GEMV of each of the step's four GEMMs (the dispatch table's form)",
                          "peak_source": f"{peak_src} hbm_gbs"},
             "e2e": e2e,
             "gpu_launches": launches_in_graphs,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
+        # the tensor-core kernel's roofline on its dominant GEMM (gate_up) of the
+        # verify and prefill steps: achieved = algorithmic bytes or flops of one
+        # launch / its in-graph time
+        for key, tkey, bound in (("verify_m16", "tc_verify_m16_gate_up", "hbm"),
+                                 ("prefill_m2048", "tc_prefill_m2048_gate_up", "tensor")):
+            e = extra.get(key)
+            if not e or "per_gemm" not in e or "gate_up" not in e["per_gemm"]:
+                continue
+            M = 16 if key == "verify_m16" else 2048
+            K, N = wi.shape_kn("gate_up")
+            us = e["per_gemm"]["gate_up"]["us"]
+            if bound == "hbm":
+                ach, pk, unit = gemm_bytes(M, K, N) / us / 1e3, hbm, "GB/s"
+            else:
+                ach, pk, unit = gemm_flops(M, K, N) / us / 1e6, bf16_peak, "TFLOP/s"
+            line[f"roofline_{key}"] = {"bound": bound, "achieved": ach, "peak": pk, "unit": unit, "frac": ach / pk,
+                                       "traffic": profiled_traffic(tkey, "dram_bytes_per_launch"),
+                                       "kernel": f"tc_gemm_kernel<{16 if M == 16 else 192}> on gate_up "
+                                                 f"{K}x{N}, M={M}", "peak_source": f"{peak_src}"}
         line.update(extra)
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -12,17 +12,20 @@
 // roles walk the same sequence of (unit, group) pairs, numbered q = 0, 1, ...
 // One pipeline stage carries one group of 128 rows of K.
 //
-//  * weight producer warp: per group, into ring stage q % SS, the packed
+//  * weight producer warp: per group, into weight stage q % SW, the packed
 //    weight slab (one bulk copy, 8 KB for a full tile) and the group's
-//    zero-point words; activation producer warp: the x tile (one 3-D TMA,
-//    two 64-wide 128-byte swizzled slabs); both complete one barrier;
+//    zero-point words; activation producer warp: into activation stage
+//    q % SX, the x tile (one 3-D TMA, two 64-wide 128-byte swizzled slabs);
 //  * dequant warpgroups (four for NT <= 64, two for NT = 128 / 192), taking groups
-//    in turn: thread t turns column t's 16 words into 64 bfloat16 pairs
-//    (q - z) -- exact small integers: mask-and-or to 128 + q, subtract
-//    128 + z -- and writes them to tensor memory as the MMA's A operand
-//    (tcgen05.st, buffer q % SA);
-//  * MMA warp: one elected lane waits for the group's one "ready" barrier (A
-//    buffer written, D buffer read out), issues its 8 tcgen05.mma kind::f16
+//    in turn: thread t copies column t's 16 words to registers (releasing
+//    the weight stage), turns them into 64 bfloat16 pairs (q - z) -- exact
+//    small integers: mask-and-or to 128 + q, subtract 128 + z -- and writes
+//    them to tensor memory as the MMA's A operand (tcgen05.st, buffer q % SA);
+//    its arrival on the group's "ready" barrier follows the activations'
+//    landing too;
+//  * two MMA warps, taking groups in turn: each waits for the group's one
+//    "ready" barrier (A buffer written, activations landed, D buffer read
+//    out), issues its 8 tcgen05.mma kind::f16
 //    (A from tensor memory, B = x from shared memory) into D buffer q % NDB
 //    and commits them to the group's barrier;
 //  * rescale warpgroup(s): per group, reads D with tcgen05.ld and adds
@@ -76,54 +79,64 @@ struct TcParams {
     int guH;         // > 0: fused gate/up weights (N = 2 guH); y[M][guH] = silu(gate) * up
 };
 
-// Configuration per token-tile width NT.  HALF: a configuration that takes at
-// most half of an SM (two dequant warpgroups, a shorter ring, 256 tensor-memory
-// columns, at most 64 registers a thread), so that two CTAs run on every SM:
-// each has its own MMA-issuing thread, and one thread issues tcgen05.mma at
-// only about half the rate an SM's tensor core sustains for small N
-// (measured: ~49 ns per M = 128, K = 16 instruction with a commit and wait
-// per group, whether one or two CTAs share the SM).
-template <int NT, bool HALF = false>
+// Groups of K per activation stage (the box of the activations' tensor map
+// spans 2 XP slabs of 64 columns).
+__host__ __device__ constexpr int tc_xp(int) { return 1; }
+
+// Configuration per token-tile width NT.  Weights (with their zero words)
+// and activations travel in two rings: a weight stage is released by the
+// dequant warps as soon as they hold its words in registers, an activation
+// stage only when the MMAs reading it are done, so the weight stream runs
+// ahead of the tensor core.  A weight stage holds WP consecutive groups of a
+// unit (one bulk copy), an activation stage XP.  Both are one: measured on
+// the decoder's shapes at M = 16, two groups per stage (one 16 KB copy for
+// two weight slabs, one TMA for two activation tiles) made the verify step
+// slower (41.4 -> 42.8 us).
+template <int NT>
 struct TcCfg {
-    static_assert(!HALF || NT <= 32, "the half-SM configuration is for small token tiles");
     static constexpr int R = NT >= 64 ? 2 : 1;           // rescale warpgroups, each owning NT/R columns
-    static constexpr int SS = HALF ? (NT <= 16 ? 8 : 6) : NT <= 16 ? 12 : NT <= 32 ? 10 : NT <= 64 ? 8 : NT <= 128 ? 4 : 3;  // shared-memory ring stages
-    static constexpr int SA = HALF ? 2 : NT <= 64 ? 4 : NT <= 128 ? 3 : 2;  // A buffers in tensor memory (q % SA)
-    static constexpr int kTmemBudget = HALF ? 256 : 512;
-    static constexpr int NDB = ((kTmemBudget - SA * 64) / NT) < 8 ? ((kTmemBudget - SA * 64) / NT) : 8;  // D accumulator ring
+    static constexpr int WP = 1;                         // groups per weight stage (1 or 2)
+    static constexpr int XP = tc_xp(NT);                 // groups per activation stage
+    static constexpr int SX = NT <= 16 ? 12 : NT <= 32 ? 10 : NT <= 64 ? 6 : NT <= 128 ? 4 : 3;  // activation stages
+    static constexpr int SW = NT <= 16 ? 16 : NT <= 32 ? 12 : NT <= 64 ? 10 : NT <= 128 ? 8 : 7;  // weight stages
+    static constexpr int SA = NT <= 64 ? 4 : NT <= 128 ? 3 : 2;  // A buffers in tensor memory (q % SA)
+    static constexpr int NDB = ((512 - SA * 64) / NT) < 8 ? ((512 - SA * 64) / NT) : 8;  // D accumulator ring
     static constexpr int kDone = 16;                     // ring of "MMAs of group q done" barriers
     // ring of "group q may be issued" barriers: its A buffer written and its D
     // buffer read out (arrivals for q follow the completion of q - SA and of
     // q - NDB, so max(SA, NDB) slots keep the phases apart)
     static constexpr int kReady = SA > NDB ? SA : NDB;
-    static constexpr int kDeqWG = HALF ? 2 : NT <= 64 ? 4 : 2;  // dequant warpgroups, taking groups q % kDeqWG
+    static constexpr int kDeqWG = NT <= 64 ? 4 : 2;     // dequant warpgroups, taking groups q % kDeqWG
     static constexpr int kDeqWarps = 4 * kDeqWG;
     static constexpr int kResWarp0 = kDeqWarps;          // rescale warpgroups follow
-    static constexpr int kMmaWarp = kDeqWarps + 4 * R;   // then the MMA warp (the only tcgen05.mma issuer)
+    static constexpr int kMmaIssuers = 2;                // MMA warps, taking groups q % 2
+    static constexpr int kMmaWarp = kDeqWarps + 4 * R;   // then the first MMA warp
     static constexpr int kProdWarp = kMmaWarp + 1;       // weight producer (also owns TMEM)
     static constexpr int kXWarp = kProdWarp + 1;         // activation producer
+    static constexpr int kMmaWarp2 = kXWarp + 1;         // the second MMA warp
     // NT >= 128: a rescale thread holds 64 or 96 f32 accumulators, more than an even
     // share of the register file allows, so the rescale warpgroups take
     // registers from the other roles (setmaxnreg).  Every role is then whole
-    // warpgroups: the last one, MMA + producers, is padded with an idle warp.
+    // warpgroups: the last one is the two MMA warps and the two producers.
     static constexpr bool kRegSplit = NT >= 128;
-    static constexpr int kWarps = kRegSplit ? (kXWarp + 4) / 4 * 4 : kXWarp + 1;
+    static constexpr int kWarps = kRegSplit ? (kMmaWarp2 + 4) / 4 * 4 : kMmaWarp2 + 1;
     static constexpr int kThreads = 32 * kWarps;
-    static constexpr int kMinBlocks = HALF ? 2 : 1;      // CTAs per SM the launch bounds ask for
     static constexpr int kRegDeq = 64, kRegRes = 144, kRegMisc = 64;  // per thread, after the split
     static constexpr int kRegPool =
         32 * (kDeqWarps * kRegDeq + 4 * R * kRegRes + (kWarps - kDeqWarps - 4 * R) * kRegMisc);
     static_assert(!kRegSplit || kRegPool <= kThreads * 96, "register split above a 96-register launch");
     static_assert(!kRegSplit || (kDeqWarps % 4 == 0 && kMmaWarp % 4 == 0), "roles must be whole warpgroups");
-    static_assert(SS <= kDone && SA <= kDone && NDB <= kDone, "barrier ring too short for the phase parity");
-    static_assert(SS + kDone + kReady + 1 <= 128, "barriers are initialised by the first threads");
+    static_assert(SX * XP < kDone && SA <= kDone && NDB <= kDone, "barrier ring too short for the phase parity");
+    static_assert(SX * XP >= 2 && SA >= 2 && NDB >= 2, "the two MMA warps' groups need distinct buffers");
+    static_assert(2 * SW + SX + kDone + kReady + 1 <= 128, "barriers are initialised by the first threads");
     // shared memory, from a 1024-byte aligned base
-    static constexpr int kXStage = NT * 256;             // two swizzled boxes of NT rows x 128 bytes
+    static constexpr int kXGroup = NT * 256;             // a group's x: two swizzled boxes of NT rows x 128 bytes
+    static constexpr int kXStage = XP * kXGroup;
     static constexpr int kXOff = 0;
-    static constexpr int kPOff = kXOff + SS * kXStage;   // packed weights, 8 KB per stage
-    static constexpr int kZOff = kPOff + SS * 8192;      // zero words, 64 bytes per stage
-    static constexpr int kSP = 6;                        // scale words each rescale thread loads ahead
-    static constexpr int kSclOff = kZOff + SS * 64;      // [kSP][128 * R] scale words (two fp16 columns each)
+    static constexpr int kPOff = kXOff + SX * kXStage;   // packed weights, 8 KB per group
+    static constexpr int kZOff = kPOff + SW * WP * 8192; // zero words, 64 bytes per group
+    static constexpr int kSP = 16;                       // scale words each rescale thread loads ahead
+    static constexpr int kSclOff = kZOff + SW * WP * 64; // [kSP][128 * R] scale words (two fp16 columns each)
     static constexpr int kBarOff = kSclOff + kSP * 128 * R * 4;
     static constexpr int kBytes = kBarOff + 1024;
     static constexpr int kAlloc = kBytes + 1024;         // slack for the alignment
@@ -133,8 +146,6 @@ struct TcCfg {
     static constexpr int kTmemUsed = SA * 64 + NDB * NT;
     static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
     static_assert(kAlloc <= 227 * 1024, "shared memory budget");
-    static_assert(!HALF || (kAlloc <= 113 * 1024 && kTmemCols <= 256 && kThreads * 64 * 2 <= 65536),
-                  "two CTAs per SM");
     static_assert(kTmemUsed <= 512, "tensor memory budget");
 };
 
@@ -181,11 +192,12 @@ W4A16_DEVICE void tmem_st_x32(uint32_t taddr, const uint32_t* v) {
         : "memory");
 }
 
-template <int NT, bool HALF>
-__global__ void __launch_bounds__(TcCfg<NT, HALF>::kThreads, TcCfg<NT, HALF>::kMinBlocks)
+template <int NT>
+__global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcParams p) {
-    using C = TcCfg<NT, HALF>;
-    constexpr int SS = C::SS;
+    using C = TcCfg<NT>;
+    constexpr int SX = C::SX;
+    constexpr int SW = C::SW;
     constexpr int SA = C::SA;
     constexpr int R = C::R;
     constexpr int ND = C::kDone;
@@ -193,8 +205,10 @@ __global__ void __launch_bounds__(TcCfg<NT, HALF>::kThreads, TcCfg<NT, HALF>::kM
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-    uint64_t* full = bars;                 // [SS] stage landed (transactions + cp.async)
-    uint64_t* done = bars + SS;            // [ND] all MMAs of group q finished: done[q % ND]
+    uint64_t* wfull = bars;                // [SW] weight stage landed (transactions + cp.async)
+    uint64_t* wempty = wfull + SW;         // [SW] weight stage read by its dequant warps
+    uint64_t* xfull = wempty + SW;         // [SX] activation stage landed
+    uint64_t* done = xfull + SX;           // [ND] all MMAs of group q finished: done[q % ND]
     // [kReady] group q may be issued: A buffer q % SA written (4 dequant warps)
     // and D buffer q % NDB read out for group q - NDB (every rescale warp)
     uint64_t* ready = done + ND;
@@ -210,14 +224,17 @@ __global__ void __launch_bounds__(TcCfg<NT, HALF>::kThreads, TcCfg<NT, HALF>::kM
     // barriers initialised in parallel, one per thread
     {
         const int i = threadIdx.x;
-        if (i < SS) mbar_init(&full[i], 2);  // one arrival per producer warp
-        else if (i < SS + ND) mbar_init(&done[i - SS], 1);
-        else if (i < SS + ND + C::kReady) mbar_init(&ready[i - SS - ND], 4 + 4 * R);
-        else if (i == SS + ND + C::kReady) {
-            mbar_init(mma_done, 1);
+        constexpr int nb = 2 * SW + SX + ND + C::kReady;  // barriers before mma_done
+        if (i < SW) mbar_init(&wfull[i], 1);              // the producer's expect-tx arrival
+        else if (i < 2 * SW) mbar_init(&wfull[i], 4 * C::WP);  // wempty: four dequant warps per group
+        else if (i < 2 * SW + SX) mbar_init(&wfull[i], 1);  // xfull: the producer's expect-tx arrival
+        else if (i < 2 * SW + SX + ND) mbar_init(&wfull[i], 1);  // done: one MMA commit
+        else if (i < nb) mbar_init(&wfull[i], 4 + 4 * R);  // ready
+        else if (i == nb) {
+            mbar_init(mma_done, C::kMmaIssuers);
             *abort_flag = 0;
         }
-        if (i <= SS + ND + C::kReady) fence_mbar_init();
+        if (i <= nb) fence_mbar_init();
     }
     if (warp == C::kProdWarp) {
         tmem_alloc(tmem_holder, C::kTmemCols);
@@ -228,7 +245,8 @@ __global__ void __launch_bounds__(TcCfg<NT, HALF>::kThreads, TcCfg<NT, HALF>::kM
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    if (warp != C::kProdWarp && warp != C::kXWarp) pdl_wait();  // producers wait in their own loops
+    // producers and rescale warps wait in their own code
+    if (warp != C::kProdWarp && warp != C::kXWarp && (warp < C::kResWarp0 || warp >= C::kMmaWarp)) pdl_wait();
 
     if (warp >= C::kMmaWarp) {
         // MMA issue, weight and activation producers, and (with the
@@ -236,110 +254,138 @@ __global__ void __launch_bounds__(TcCfg<NT, HALF>::kThreads, TcCfg<NT, HALF>::kM
         if constexpr (C::kRegSplit) regs_dec<C::kRegMisc>();
         if (warp == C::kProdWarp) {
             // ------------------------------------------------ weight producer
-            // Per group, into ring stage q % SS: the packed weight slab and the
-            // zero-point words.  The zero words are 16-byte aligned when
-            // N % 32 == 0 and then come in one bulk copy; otherwise lane 0 fetches
-            // them with 4-byte async copies.
-            int q = 0, issued = 0;
+            // Per weight stage (two consecutive groups of a unit, or a unit's
+            // last group alone): the packed weight slabs in one bulk copy and
+            // the groups' zero-point words, fetched by the lanes with 4-byte
+            // asynchronous copies (lanes 16 i + c: word c of the stage's group i).
+            static_assert(C::WP == 1 || C::WP == 2, "lanes 16 i + c serve group i of a stage");
+            int wbase = 0, issued = 0;  // flat index of the unit's first weight stage; stages armed
             bool ok = true;
-            // (fused gate/up weights: a tile's zero words come from two places)
-            const bool zbulk = !p.guH && p.N % 32 == 0;
             // This warp touches only weights and zeros: with static weights it
             // never waits on the preceding grid, otherwise once before any load.
             if (!p.prefetch) pdl_wait();
             for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
                 const UnitInfo ui = unit_info(p, u);
                 const int W = L.width(ui.nb);
-                const uint32_t wbytes = (uint32_t)W * 64;
-                const uint32_t zbytes = zbulk ? (uint32_t)(W / 2) : 0u;
+                const int Gu = ui.g1 - ui.g0;
                 const uint32_t* wsrc = p.qd + L.block_word(ui.nb, ui.g0);
                 const uint32_t* zsrc = p.qzeros + (size_t)ui.g0 * (p.N / 8) + 16 * ui.nb;
-                for (int g = ui.g0; g < ui.g1; ++g, ++q, wsrc += W * 16, zsrc += p.N / 8) {
-                    const int s = q % SS;
-                    // stage s is free once the MMAs of group q - SS are done
-                    if (ok && q >= SS &&
-                        !mbar_wait_warp(&done[(q - SS) % ND], ((q - SS) / ND) & 1, abort_flag, &g_tc_status))
+                for (int j = 0; j < Gu; j += C::WP) {
+                    const int pw = wbase + j / C::WP;
+                    const int s = pw % SW;
+                    const int n = Gu - j < C::WP ? Gu - j : C::WP;
+                    // stage s is free once the dequant warps of its previous groups hold their words
+                    if (ok && pw >= SW &&
+                        !mbar_wait_warp(&wempty[s], ((pw - SW) / SW) & 1, abort_flag, &g_tc_status))
                         ok = false;
                     if (ok) {
-                        if (!zbulk && lane < W / 8) {  // one zero word per lane
-                            const int zi = p.guH ? (gu_column(128 * ui.nb + 8 * lane, p.guH) >> 3) - 16 * ui.nb : lane;
-                            cp_async_4(smem + C::kZOff + s * 64 + lane * 4, zsrc + zi);
-                            cp_async_mbar_arrive(&full[s]);
+                        const int zg = lane >> 4, zc = lane & 15;
+                        if (zg < n && zc < W / 8) {
+                            // (fused gate/up weights: a tile's zero words come from two places)
+                            const int zi = p.guH ? (gu_column(128 * ui.nb + 8 * zc, p.guH) >> 3) - 16 * ui.nb : zc;
+                            cp_async_4(smem + C::kZOff + (s * C::WP + zg) * 64 + zc * 4,
+                                       zsrc + (size_t)(j + zg) * (p.N / 8) + zi);
+                            cp_async_mbar_arrive(&wfull[s]);
                         }
                         __syncwarp();  // every lane's pending arrival precedes the expected-bytes arrival
                         if (lane == 0) {
-                            mbar_arrive_expect_tx(&full[s], wbytes + zbytes);
-                            bulk_g2s(smem + C::kPOff + s * 8192, wsrc, wbytes, &full[s]);
-                            if (zbulk) bulk_g2s(smem + C::kZOff + s * 64, zsrc, zbytes, &full[s]);
+                            const uint32_t bytes = (uint32_t)(n * W * 64);
+                            mbar_arrive_expect_tx(&wfull[s], bytes);
+                            bulk_g2s(smem + C::kPOff + s * (C::WP * 8192), wsrc + (size_t)j * W * 16, bytes, &wfull[s]);
                         }
                         __syncwarp();
-                        issued = q + 1;
+                        issued = pw + 1;
                     }
                 }
+                wbase += (Gu + C::WP - 1) / C::WP;
             }
             // drain: every stage armed must land before the CTA may exit
-            for (int i = issued > SS ? issued - SS : 0; i < issued; ++i)
-                (void)mbar_wait(&full[i % SS], (i / SS) & 1, nullptr, &g_tc_status);
+            for (int i = issued > SW ? issued - SW : 0; i < issued; ++i)
+                (void)mbar_wait(&wfull[i % SW], (i / SW) & 1, nullptr, &g_tc_status);
         } else if (warp == C::kXWarp) {
             // -------------------------------------------- activation producer
-            // Per group: x[tile tokens][128 rows of K] with one 3-D TMA (two
-            // 64-wide, 128-byte swizzled slabs).  Always after the preceding grid.
+            // Per activation stage (XP consecutive groups of a unit, or fewer at
+            // its end): x[tile tokens][128 XP rows of K] with one 3-D TMA
+            // (64-wide, 128-byte swizzled slabs; slabs past K read as zeros).
+            // Always after the preceding grid.  A stage is refilled once the
+            // MMAs of every group it held are done.
             pdl_wait();
-            int q = 0, issued = 0;
+            int xbase = 0, issued = 0, q = 0;
+            int qwaited = 0;   // groups before this one have had their "done" waited on
+            int rend[SX];      // per stage: the flat index one past its last group
             bool ok = true;
             for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
                 const UnitInfo ui = unit_info(p, u);
-                for (int g = ui.g0; g < ui.g1; ++g, ++q) {
-                    const int s = q % SS;
-                    if (ok && q >= SS &&
-                        !mbar_wait_warp(&done[(q - SS) % ND], ((q - SS) / ND) & 1, abort_flag, &g_tc_status))
-                        ok = false;
+                const int Gu = ui.g1 - ui.g0;
+                for (int j = 0; j < Gu; j += C::XP) {
+                    const int px = xbase + j / C::XP;
+                    const int s = px % SX;
+                    const int n = Gu - j < C::XP ? Gu - j : C::XP;
+                    if (px >= SX)
+                        for (; ok && qwaited < rend[s]; ++qwaited)
+                            if (!mbar_wait_warp(&done[qwaited % ND], (qwaited / ND) & 1, abort_flag, &g_tc_status))
+                                ok = false;
                     if (ok) {
                         if (lane == 0) {
-                            mbar_arrive_expect_tx(&full[s], (uint32_t)C::kXStage);
-                            tma_load_3d(smem + C::kXOff + s * C::kXStage, &tmap_x, 0, ui.mb * NT, 2 * g, &full[s]);
+                            mbar_arrive_expect_tx(&xfull[s], (uint32_t)C::kXStage);
+                            tma_load_3d(smem + C::kXOff + s * C::kXStage, &tmap_x, 0, ui.mb * NT, 2 * (ui.g0 + j),
+                                        &xfull[s]);
                         }
                         __syncwarp();
-                        issued = q + 1;
+                        rend[s] = q + j + n;
+                        issued = px + 1;
                     }
                 }
+                q += Gu;
+                xbase += (Gu + C::XP - 1) / C::XP;
             }
-            for (int i = issued > SS ? issued - SS : 0; i < issued; ++i)
-                (void)mbar_wait(&full[i % SS], (i / SS) & 1, nullptr, &g_tc_status);
-        } else if (warp == C::kMmaWarp) {
+            for (int i = issued > SX ? issued - SX : 0; i < issued; ++i)
+                (void)mbar_wait(&xfull[i % SX], (i / SX) & 1, nullptr, &g_tc_status);
+        } else if (warp == C::kMmaWarp || warp == C::kMmaWarp2) {
             // ------------------------------------------------------------ MMA issue
-            // The one thread of the CTA that issues tcgen05.mma: the whole loop runs
-            // in an elected lane, so a barrier that has already completed costs a
-            // single poll and no warp vote.  It needs only the flat group index q.
+            // Two MMA warps take the groups in turn, q % 2.  Each runs its loop
+            // with all 32 lanes (operands computed by the warp, each instruction
+            // issued by one elected lane).  Measured on GB300 at M = 128, N = 16:
+            // a warp that waits on a barrier between its groups of 8 MMAs issues
+            // one every ~32 ns, whatever the depth it waits at (each wait costs
+            // ~190 ns), and two such warps on one SM one every ~16 ns between
+            // them; a single lane running the loop alone, one every ~47 ns.
+            // Groups q and q + 1 use different A and D buffers and x stages
+            // (SA, NDB >= 2), so the two warps' MMAs never touch the same
+            // tensor memory; each commit covers the MMAs of its own warp.
             constexpr uint32_t idesc = idesc_bf16_f32(128, NT);
-            int Q = 0;  // groups this CTA processes
-            for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+            const int w = warp == C::kMmaWarp ? 0 : 1;
+            int q = 0, xbase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
                 const UnitInfo ui = unit_info(p, u);
-                Q += ui.g1 - ui.g0;
-            }
-            if (elect_one()) {
-                bool ok = true;
-                for (int q = 0; q < Q; ++q) {
-                    // A buffer q % SA written and D buffer q % NDB free: one poll
-                    if (!mbar_wait(&ready[q % C::kReady], (q / C::kReady) & 1, abort_flag, &g_tc_status)) ok = false;
-                    if (!ok) {
+                const int Gu = ui.g1 - ui.g0;
+                for (int j = 0; j < Gu; ++j, ++q) {
+                    if ((q % C::kMmaIssuers) != w) continue;
+                    // A buffer q % SA written, activations landed, D buffer q % NDB free
+                    if (!mbar_wait_warp(&ready[q % C::kReady], (q / C::kReady) & 1, abort_flag, &g_tc_status)) {
                         *abort_flag = 1;
+                        ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t xaddr = smem_u32(smem + C::kXOff + (q % SS) * C::kXStage);
+                    const int px = xbase + j / C::XP;
+                    const uint32_t xaddr =
+                        smem_u32(smem + C::kXOff + (px % SX) * C::kXStage + (j % C::XP) * C::kXGroup);
                     const uint32_t a_tmem = tmem + C::kTmemA + (q % SA) * 64;
                     const uint32_t d_tmem = tmem + C::kTmemD + (q % C::NDB) * NT;
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t bdesc = smem_desc_sw128(xaddr + (kk >> 2) * (NT * 128) + (kk & 3) * 32);
-                        mma_bf16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+                        mma_bf16_ts_warp(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(&done[q % ND]);
+                    mma_commit_warp(&done[q % ND]);
                 }
-                // every MMA issued must be complete before TMEM is freed
-                mma_commit(mma_done);
+                xbase += (Gu + C::XP - 1) / C::XP;
             }
+            // every MMA issued must be complete before TMEM is freed (both
+            // warps arrive on mma_done)
+            mma_commit_warp(mma_done);
             __syncwarp();
             pdl_launch_dependents();  // this CTA issues no more tensor work
             (void)mbar_wait(mma_done, 0, nullptr, &g_tc_status);
@@ -351,28 +397,44 @@ __global__ void __launch_bounds__(TcCfg<NT, HALF>::kThreads, TcCfg<NT, HALF>::kM
         const int quad = warp & 3;            // TMEM lane quadrant
         const int t = quad * 32 + lane;       // A row = tile column
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        int q = 0;
+        int q = 0, wbase = 0, xbase = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const UnitInfo ui = unit_info(p, u);
             const int W = L.width(ui.nb);
+            const int Gu = ui.g1 - ui.g0;
             // columns beyond a ragged tile read column W-1; their A rows only
             // feed D rows that are never written out
             const int tc = t < W ? t : W - 1;
-            for (int g = ui.g0; g < ui.g1; ++g, ++q) {
+            for (int j = 0; j < Gu; ++j, ++q) {
                 if ((q % C::kDeqWG) != h) continue;
-                const int s = q % SS;
-                if (ok && !mbar_wait_warp(&full[s], (q / SS) & 1, abort_flag, &g_tc_status)) ok = false;
-                // first half computed before waiting for the A buffer, so the
-                // ALU work overlaps the previous group's MMAs
-                const uint32_t zs = smem_u32(smem + C::kZOff + s * 64);
-                const uint32_t src = smem_u32(smem + C::kPOff + s * 8192);
+                const int pw = wbase + j / C::WP, slot = j % C::WP;
+                const int s = pw % SW;
+                const bool alone = Gu - (j - slot) < C::WP;  // the stage holds this group only
+                if (ok && !mbar_wait_warp(&wfull[s], (pw / SW) & 1, abort_flag, &g_tc_status)) ok = false;
+                // the column's 128 codes (four 16-byte words) and its zero point
+                // into registers, then the group's share of the weight stage goes
+                // back to the producer
+                uint4 wq[4];
                 uint32_t zz = 0x43004300u;
+                if (ok) {
+                    const uint32_t src = smem_u32(smem + C::kPOff + s * (C::WP * 8192) + slot * W * 64);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) wq[c] = lds_v4(src + (uint32_t)((c * W + tc) * 16));
+                    const uint32_t zs = smem_u32(smem + C::kZOff + (s * C::WP + slot) * 64);
+                    const uint32_t z = (lds_u32(zs + (uint32_t)((tc >> 3) * 4)) >> (4 * (tc & 7))) & 0xFu;
+                    zz = 0x43004300u | z | (z << 16);  // bfloat16 pair (128 + z, 128 + z)
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&wempty[s]);
+                        if (alone) mbar_arrive(&wempty[s]);  // the absent group's share
+                    }
+                }
                 uint32_t a[32];
                 auto dequant_half = [&](int half) {
 #pragma unroll
                     for (int cl = 0; cl < 2; ++cl) {
-                        const uint4 v = lds_v4(src + (uint32_t)(((2 * half + cl) * W + tc) * 16));
+                        const uint4 v = wq[2 * half + cl];
                         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
@@ -380,11 +442,9 @@ __global__ void __launch_bounds__(TcCfg<NT, HALF>::kThreads, TcCfg<NT, HALF>::kM
                             for (int pp = 0; pp < 4; ++pp) a[16 * cl + 4 * j + pp] = bf16x2_sub(magic_pair(wv[j], pp), zz);
                     }
                 };
-                if (ok) {
-                    const uint32_t z = (lds_u32(zs + (uint32_t)((tc >> 3) * 4)) >> (4 * (tc & 7))) & 0xFu;
-                    zz = 0x43004300u | z | (z << 16);  // bfloat16 pair (128 + z, 128 + z)
-                    dequant_half(0);
-                }
+                // first half computed before waiting for the A buffer, so the
+                // ALU work overlaps the previous group's MMAs
+                if (ok) dequant_half(0);
                 // A buffer q % SA is free once the MMAs of group q - SA are done
                 if (ok && q >= SA &&
                     !mbar_wait_warp(&done[(q - SA) % ND], ((q - SA) / ND) & 1, abort_flag, &g_tc_status))
@@ -397,12 +457,20 @@ __global__ void __launch_bounds__(TcCfg<NT, HALF>::kThreads, TcCfg<NT, HALF>::kM
                     dequant_half(1);
                     tmem_st_x32(abase + 32, a);
                     tmem_wait_st();
+                }
+                // the group's activations have landed: the MMA warp, which waits
+                // only for "ready", reads them after this arrival
+                const int px = xbase + j / C::XP;
+                if (ok && !mbar_wait_warp(&xfull[px % SX], (px / SX) & 1, abort_flag, &g_tc_status)) ok = false;
+                if (ok) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&ready[q % C::kReady]);
                 }
                 if (!ok) *abort_flag = 1;
             }
+            wbase += (Gu + C::WP - 1) / C::WP;
+            xbase += (Gu + C::XP - 1) / C::XP;
         }
     } else {
         if constexpr (C::kRegSplit) regs_inc<C::kRegRes>();
@@ -444,8 +512,17 @@ __global__ void __launch_bounds__(TcCfg<NT, HALF>::kThreads, TcCfg<NT, HALF>::kM
             }
             cp_async_commit();  // possibly empty: keeps one group per slot
         };
+        // scales are weights: with static weights the first loads go out
+        // before the preceding grid completes
+        if (p.prefetch) {
 #pragma unroll 1
-        for (int i = 0; i < C::kSP; ++i) issue_scale(i);
+            for (int i = 0; i < C::kSP; ++i) issue_scale(i);
+            pdl_wait();
+        } else {
+            pdl_wait();
+#pragma unroll 1
+            for (int i = 0; i < C::kSP; ++i) issue_scale(i);
+        }
         // the D buffers of the first NDB groups start out free
         if (lane == 0)
             for (int i = 0; i < C::NDB; ++i) mbar_arrive(&ready[i]);
@@ -619,11 +696,6 @@ __global__ void __launch_bounds__(TcCfg<NT, HALF>::kThreads, TcCfg<NT, HALF>::kM
 // 192-token tiles: two D buffers of 192 columns still fit beside two A
 // buffers in the 512 tensor-memory columns.
 static int tc_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 256 ? 128 : 192; }
-// Token tiles of up to kTcHalfMaxNT tokens run the half-SM configuration,
-// two CTAs per SM.  Off: measured at M = 16 and 32 on the decoder's shapes it
-// was slower (verify step 40.7 -> 46.9 us), the two CTAs sharing the SM's copy
-// engine, which the three copies per group already keep busy.
-constexpr int kTcHalfMaxNT = 0;
 
 bool tc_plan(int M, int N, int K, int sms, TcPlan* out, int force_nt) {
     const Layout L(K, N);
@@ -633,17 +705,16 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out, int force_nt) {
     const int table_nt = force_nt ? 0 : dispatch_nt(M, K, N);
     const int NT = force_nt ? force_nt : table_nt ? table_nt : tc_nt(M);
     const int MT = (M + NT - 1) / NT;
-    const bool half = NT <= kTcHalfMaxNT;
-    const long long slots = half ? 2ll * sms : sms;  // CTAs resident at once
+    const long long slots = sms;  // CTAs resident at once, one per SM
     const long long tiles = (long long)L.NB * MT;
     const int max_split = G / 2 > 0 ? G / 2 : 1;  // at least 2 groups a piece
     long long whole = tiles;
-    // Pieces of a partial last round only for long K (at least 48 groups),
-    // at least 8 groups each: measured at M = 2048, cutting the tail of
-    // 9728-deep tiles saved 8 % while cutting 2560- and 4096-deep tiles
-    // (pieces of 4 to 10 groups) cost 10 %, the pieces' reduction
-    // outweighing the balance.
-    const int max_split_tail = G >= 48 ? G / 8 : 1;
+    // Pieces of a partial last round for K of at least 16 groups, at least 5
+    // groups each.  Measured at M = 2048 with the token-major partials: the
+    // 4096-deep tiles of o_proj 50.1 -> 45.9 us (two pieces), the 2560-deep
+    // tiles of qkv unchanged (three pieces), the 9728-deep ones of down as
+    // with pieces of 8 or more.
+    const int max_split_tail = G >= 16 ? G / 5 : 1;
     int splits = 1;
     if (tiles < slots) {
         // Fewer tiles than CTAs: every tile in K pieces, rounded down so that
@@ -676,9 +747,8 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out, int force_nt) {
     out->splits = splits;
     out->units = (int)units;
     out->ctas = (int)(units < slots ? units : slots);
-    out->half = half;
-    out->smem = NT == 16    ? (half ? TcCfg<16, true>::kAlloc : TcCfg<16>::kAlloc)
-                : NT == 32  ? (half ? TcCfg<32, true>::kAlloc : TcCfg<32>::kAlloc)
+    out->smem = NT == 16    ? TcCfg<16>::kAlloc
+                : NT == 32  ? TcCfg<32>::kAlloc
                 : NT == 64  ? TcCfg<64>::kAlloc
                 : NT == 128 ? TcCfg<128>::kAlloc
                             : TcCfg<192>::kAlloc;
@@ -704,11 +774,11 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-template <int NT, bool HALF = false>
+template <int NT>
 static cudaError_t launch_nt(const CUtensorMap& tm, const TcParams& prm, const TcPlan& plan, cudaStream_t s,
                              bool pdl) {
-    using C = TcCfg<NT, HALF>;
-    auto kern = tc_gemm_kernel<NT, HALF>;
+    using C = TcCfg<NT>;
+    auto kern = tc_gemm_kernel<NT>;
     static int set_for[64];  // shared memory limit raised once per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -730,6 +800,7 @@ static cudaError_t launch_nt(const CUtensorMap& tm, const TcParams& prm, const T
     return launch_kernel(kern, dim3(plan.ctas), dim3(C::kThreads), plan.smem, s, pdl, tm, prm);
 }
 
+
 cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
                       uint16_t* y, int M, int N, int K, void* ws, const TcPlan& plan, cudaStream_t s,
                       unsigned flags, int guH) {
@@ -737,10 +808,10 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
     if (!encode) return cudaErrorNotSupported;
     CUtensorMap tm;
     // x viewed as [K/64 slabs][M tokens][64 columns]: one box is NT tokens x
-    // two slabs of 64 columns, i.e. one group of 128 rows of K
+    // 2 XP slabs of 64 columns, i.e. XP groups of 128 rows of K
     const cuuint64_t dims[3] = {64, (cuuint64_t)M, (cuuint64_t)(K / 64)};
     const cuuint64_t strides[2] = {(cuuint64_t)K * 2, 128};
-    const cuuint32_t box[3] = {64, (cuuint32_t)plan.NT, 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)plan.NT, (cuuint32_t)(2 * tc_xp(plan.NT))};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(x), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -767,8 +838,8 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     prm.guH = guH;
     switch (plan.NT) {
-        case 16: return plan.half ? launch_nt<16, true>(tm, prm, plan, s, pdl) : launch_nt<16>(tm, prm, plan, s, pdl);
-        case 32: return plan.half ? launch_nt<32, true>(tm, prm, plan, s, pdl) : launch_nt<32>(tm, prm, plan, s, pdl);
+        case 16: return launch_nt<16>(tm, prm, plan, s, pdl);
+        case 32: return launch_nt<32>(tm, prm, plan, s, pdl);
         case 64: return launch_nt<64>(tm, prm, plan, s, pdl);
         case 192: return launch_nt<192>(tm, prm, plan, s, pdl);
         default: return launch_nt<128>(tm, prm, plan, s, pdl);

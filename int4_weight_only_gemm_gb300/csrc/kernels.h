@@ -77,7 +77,6 @@ struct TcPlan {
     int whole, splits;       // tiles [0, whole) whole, the rest in `splits` K pieces each
     int units;               // whole + (NB * MT - whole) * splits
     int ctas;                // persistent CTAs
-    bool half;               // the half-SM configuration, two CTAs per SM
     size_t smem, ws_bytes;
 };
 // force_nt: a token tile (16, 32, 64, 128 or 192) in place of the table's, 0 = the table's
@@ -86,22 +85,38 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
                       uint16_t* y, int M, int N, int K, void* ws, const TcPlan& plan, cudaStream_t s,
                       unsigned flags, int guH);
 
-// Launch `kern` with an optional programmatic-stream-serialization attribute.
+// Launch `kern` with an optional programmatic-stream-serialization attribute
+// and, for cluster > 1, clusters of `cluster` CTAs along x.
 template <typename Kern, typename... Args>
-cudaError_t launch_kernel(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, Args... args) {
+cudaError_t launch_kernel_ex(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, int cluster,
+                             Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
     if (pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
     }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_kernel(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, Args... args) {
+    return launch_kernel_ex(kern, grid, block, smem, s, pdl, 0, args...);
 }
 int tc_read_status();
 
