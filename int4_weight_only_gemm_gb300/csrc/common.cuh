@@ -185,6 +185,11 @@ W4A16_DEVICE uint32_t lds_u32(uint32_t addr) {
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
 }
+W4A16_DEVICE unsigned short lds_u16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
 
 // ---------------------------------------------------------------------------
 // bulk and tensor copies (TMA), global -> shared, completion on an mbarrier

@@ -77,21 +77,27 @@ struct TcParams {
     int units;       // whole + (tiles - whole) * splits
     int prefetch;    // weights may be loaded before the preceding grid completes
     int guH;         // > 0: fused gate/up weights (N = 2 guH); y[M][guH] = silu(gate) * up
+    int zmap;        // tmap_z describes the zero words (N % 32 == 0); otherwise the lanes copy them
 };
 
 // Groups of K per activation stage (the box of the activations' tensor map
 // spans 2 XP slabs of 64 columns).
 __host__ __device__ constexpr int tc_xp(int) { return 1; }
 
-// Configuration per token-tile width NT.  Weights (with their zero words)
-// and activations travel in two rings: a weight stage is released by the
+// Configuration per token-tile width NT.  Weights and activations travel in
+// two rings: a weight stage is released by the
 // dequant warps as soon as they hold its words in registers, an activation
 // stage only when the MMAs reading it are done, so the weight stream runs
 // ahead of the tensor core.  A weight stage holds WP consecutive groups of a
 // unit (one bulk copy), an activation stage XP.  Both are one: measured on
 // the decoder's shapes at M = 16, two groups per stage (one 16 KB copy for
 // two weight slabs, one TMA for two activation tiles) made the verify step
-// slower (41.4 -> 42.8 us).
+// slower (41.4 -> 42.8 us).  The groups' scales and zero words arrive in
+// chunks of GB groups (four 2-D tensor copies per chunk, MB chunk buffers),
+// issued by the weight producer as it enters a chunk and released by the
+// rescale warps after the chunk's last group: measured, per-thread 4-byte
+// scale loads kept 16 deep stalled the rescale warps for ~2 us at the start
+// and ~0.3 us per group while the weight stream saturated the memory system.
 template <int NT>
 struct TcCfg {
     static constexpr int R = NT >= 64 ? 2 : 1;           // rescale warpgroups, each owning NT/R columns
@@ -106,6 +112,8 @@ struct TcCfg {
     // buffer read out (arrivals for q follow the completion of q - SA and of
     // q - NDB, so max(SA, NDB) slots keep the phases apart)
     static constexpr int kReady = SA > NDB ? SA : NDB;
+    static constexpr int GB = 16;                        // groups per metadata chunk
+    static constexpr int MB = 3;                         // metadata chunk buffers
     static constexpr int kDeqWG = NT <= 64 ? 4 : 2;     // dequant warpgroups, taking groups q % kDeqWG
     static constexpr int kDeqWarps = 4 * kDeqWG;
     static constexpr int kResWarp0 = kDeqWarps;          // rescale warpgroups follow
@@ -128,16 +136,20 @@ struct TcCfg {
     static_assert(!kRegSplit || (kDeqWarps % 4 == 0 && kMmaWarp % 4 == 0), "roles must be whole warpgroups");
     static_assert(SX * XP < kDone && SA <= kDone && NDB <= kDone, "barrier ring too short for the phase parity");
     static_assert(SX * XP >= 2 && SA >= 2 && NDB >= 2, "the two MMA warps' groups need distinct buffers");
-    static_assert(2 * SW + SX + kDone + kReady + 1 <= 128, "barriers are initialised by the first threads");
+    static_assert(2 * SW + SX + 2 * MB + kDone + kReady + 1 <= 128, "barriers are initialised by the first threads");
+    static_assert(GB % WP == 0, "a weight stage never straddles two metadata chunks");
     // shared memory, from a 1024-byte aligned base
     static constexpr int kXGroup = NT * 256;             // a group's x: two swizzled boxes of NT rows x 128 bytes
     static constexpr int kXStage = XP * kXGroup;
     static constexpr int kXOff = 0;
     static constexpr int kPOff = kXOff + SX * kXStage;   // packed weights, 8 KB per group
-    static constexpr int kZOff = kPOff + SW * WP * 8192; // zero words, 64 bytes per group
-    static constexpr int kSP = 16;                       // scale words each rescale thread loads ahead
-    static constexpr int kSclOff = kZOff + SW * WP * 64; // [kSP][128 * R] scale words (two fp16 columns each)
-    static constexpr int kBarOff = kSclOff + kSP * 128 * R * 4;
+    // metadata chunk: scales [2 boxes][GB groups][64 columns] fp16, then zero
+    // words [2 boxes][GB groups][8 words]; box 0 / 1 = the tile's first / second
+    // 64 columns (fused gate/up weights: its gate / up columns)
+    static constexpr int kMetaScl = 2 * GB * 64 * 2;
+    static constexpr int kMetaBytes = kMetaScl + 2 * GB * 8 * 4;
+    static constexpr int kMetaOff = kPOff + SW * WP * 8192;
+    static constexpr int kBarOff = kMetaOff + MB * kMetaBytes;
     static constexpr int kBytes = kBarOff + 1024;
     static constexpr int kAlloc = kBytes + 1024;         // slack for the alignment
     // tensor memory: SA A-buffers of 64 columns, then the D ring of NDB x NT columns
@@ -194,7 +206,8 @@ W4A16_DEVICE void tmem_st_x32(uint32_t taddr, const uint32_t* v) {
 
 template <int NT>
 __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcParams p) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_s,
+                   const __grid_constant__ CUtensorMap tmap_z, const TcParams p) {
     using C = TcCfg<NT>;
     constexpr int SX = C::SX;
     constexpr int SW = C::SW;
@@ -208,7 +221,9 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
     uint64_t* wfull = bars;                // [SW] weight stage landed (transactions + cp.async)
     uint64_t* wempty = wfull + SW;         // [SW] weight stage read by its dequant warps
     uint64_t* xfull = wempty + SW;         // [SX] activation stage landed
-    uint64_t* done = xfull + SX;           // [ND] all MMAs of group q finished: done[q % ND]
+    uint64_t* mfull = xfull + SX;          // [MB] metadata chunk landed
+    uint64_t* mempty = mfull + C::MB;      // [MB] metadata chunk used up by the rescale warps
+    uint64_t* done = mempty + C::MB;       // [ND] all MMAs of group q finished: done[q % ND]
     // [kReady] group q may be issued: A buffer q % SA written (4 dequant warps)
     // and D buffer q % NDB read out for group q - NDB (every rescale warp)
     uint64_t* ready = done + ND;
@@ -224,11 +239,14 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
     // barriers initialised in parallel, one per thread
     {
         const int i = threadIdx.x;
-        constexpr int nb = 2 * SW + SX + ND + C::kReady;  // barriers before mma_done
+        constexpr int MB = C::MB;
+        constexpr int nb = 2 * SW + SX + 2 * MB + ND + C::kReady;  // barriers before mma_done
         if (i < SW) mbar_init(&wfull[i], 1);              // the producer's expect-tx arrival
         else if (i < 2 * SW) mbar_init(&wfull[i], 4 * C::WP);  // wempty: four dequant warps per group
         else if (i < 2 * SW + SX) mbar_init(&wfull[i], 1);  // xfull: the producer's expect-tx arrival
-        else if (i < 2 * SW + SX + ND) mbar_init(&wfull[i], 1);  // done: one MMA commit
+        else if (i < 2 * SW + SX + MB) mbar_init(&wfull[i], 1);  // mfull: the producer's expect-tx arrival
+        else if (i < 2 * SW + SX + 2 * MB) mbar_init(&wfull[i], 4 * R);  // mempty: every rescale warp
+        else if (i < 2 * SW + SX + 2 * MB + ND) mbar_init(&wfull[i], 1);  // done: one MMA commit
         else if (i < nb) mbar_init(&wfull[i], 4 + 4 * R);  // ready
         else if (i == nb) {
             mbar_init(mma_done, C::kMmaIssuers);
@@ -239,14 +257,17 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
     if (warp == C::kProdWarp) {
         tmem_alloc(tmem_holder, C::kTmemCols);
         tmem_relinquish();
-        if (lane == 0) prefetch_tmap(&tmap_x);
+        if (lane == 0) {
+            prefetch_tmap(&tmap_x);
+            prefetch_tmap(&tmap_s);
+            if (p.zmap) prefetch_tmap(&tmap_z);
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    // producers and rescale warps wait in their own code
-    if (warp != C::kProdWarp && warp != C::kXWarp && (warp < C::kResWarp0 || warp >= C::kMmaWarp)) pdl_wait();
+    if (warp != C::kProdWarp && warp != C::kXWarp) pdl_wait();  // producers wait in their own loops
 
     if (warp >= C::kMmaWarp) {
         // MMA issue, weight and activation producers, and (with the
@@ -254,23 +275,65 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
         if constexpr (C::kRegSplit) regs_dec<C::kRegMisc>();
         if (warp == C::kProdWarp) {
             // ------------------------------------------------ weight producer
-            // Per weight stage (two consecutive groups of a unit, or a unit's
-            // last group alone): the packed weight slabs in one bulk copy and
-            // the groups' zero-point words, fetched by the lanes with 4-byte
-            // asynchronous copies (lanes 16 i + c: word c of the stage's group i).
-            static_assert(C::WP == 1 || C::WP == 2, "lanes 16 i + c serve group i of a stage");
-            int wbase = 0, issued = 0;  // flat index of the unit's first weight stage; stages armed
+            // Per weight stage (WP consecutive groups of a unit): the packed
+            // weight slabs in one bulk copy.  On entering a metadata chunk (GB
+            // groups of a unit), first the chunk's scales and zero words: 2-D
+            // tensor copies of GB rows x 64 columns (two per array), or, for
+            // zero words whose rows are not 16-byte aligned (N % 32 != 0),
+            // 4-byte asynchronous copies by the lanes.
+            constexpr int GB = C::GB, MB = C::MB;
+            int wbase = 0, cbase = 0, issued = 0, missued = 0;  // first stage / chunk of the unit; armed
             bool ok = true;
-            // This warp touches only weights and zeros: with static weights it
-            // never waits on the preceding grid, otherwise once before any load.
+            // This warp touches only weights, scales and zeros: with static
+            // weights it never waits on the preceding grid, otherwise once
+            // before any load.
             if (!p.prefetch) pdl_wait();
             for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
                 const UnitInfo ui = unit_info(p, u);
                 const int W = L.width(ui.nb);
                 const int Gu = ui.g1 - ui.g0;
                 const uint32_t* wsrc = p.qd + L.block_word(ui.nb, ui.g0);
-                const uint32_t* zsrc = p.qzeros + (size_t)ui.g0 * (p.N / 8) + 16 * ui.nb;
                 for (int j = 0; j < Gu; j += C::WP) {
+                    if (j % GB == 0) {
+                        const int c = cbase + j / GB;
+                        const int ms = c % MB;
+                        // buffer ms is free once the rescale warps are done with chunk c - MB
+                        if (ok && c >= MB &&
+                            !mbar_wait_warp(&mempty[ms], ((c - MB) / MB) & 1, abort_flag, &g_tc_status))
+                            ok = false;
+                        if (ok) {
+                            unsigned char* mbuf = smem + C::kMetaOff + ms * C::kMetaBytes;
+                            const int g = ui.g0 + j;
+                            if (!p.zmap) {
+                                // word w of box b, row r: canonical zero word zw(b) + w of group g + r
+                                const int zw0 = p.guH ? 8 * ui.nb : 16 * ui.nb;
+                                const int zw1 = p.guH ? p.guH / 8 + 8 * ui.nb : 16 * ui.nb + 8;
+                                for (int i = lane; i < 2 * GB * 8; i += 32) {
+                                    const int b = i / (GB * 8), r = (i / 8) % GB, w = i % 8;
+                                    const int zw = (b ? zw1 : zw0) + w;
+                                    if (g + r < ui.g1 && zw < p.N / 8)
+                                        cp_async_4(mbuf + C::kMetaScl + i * 4, p.qzeros + (size_t)(g + r) * (p.N / 8) + zw);
+                                }
+                                cp_async_mbar_arrive(&mfull[ms]);
+                            }
+                            __syncwarp();  // every lane's pending arrival precedes the expected-bytes arrival
+                            if (lane == 0) {
+                                mbar_arrive_expect_tx(&mfull[ms], (uint32_t)(p.zmap ? C::kMetaBytes : C::kMetaScl));
+                                const int sx0 = p.guH ? 64 * ui.nb : 128 * ui.nb;
+                                const int sx1 = p.guH ? p.guH + 64 * ui.nb : 128 * ui.nb + 64;
+                                tma_load_2d(mbuf, &tmap_s, sx0, g, &mfull[ms]);
+                                tma_load_2d(mbuf + GB * 64 * 2, &tmap_s, sx1, g, &mfull[ms]);
+                                if (p.zmap) {
+                                    const int zx0 = p.guH ? 8 * ui.nb : 16 * ui.nb;
+                                    const int zx1 = p.guH ? p.guH / 8 + 8 * ui.nb : 16 * ui.nb + 8;
+                                    tma_load_2d(mbuf + C::kMetaScl, &tmap_z, zx0, g, &mfull[ms]);
+                                    tma_load_2d(mbuf + C::kMetaScl + GB * 8 * 4, &tmap_z, zx1, g, &mfull[ms]);
+                                }
+                            }
+                            __syncwarp();
+                            missued = c + 1;
+                        }
+                    }
                     const int pw = wbase + j / C::WP;
                     const int s = pw % SW;
                     const int n = Gu - j < C::WP ? Gu - j : C::WP;
@@ -279,15 +342,6 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                         !mbar_wait_warp(&wempty[s], ((pw - SW) / SW) & 1, abort_flag, &g_tc_status))
                         ok = false;
                     if (ok) {
-                        const int zg = lane >> 4, zc = lane & 15;
-                        if (zg < n && zc < W / 8) {
-                            // (fused gate/up weights: a tile's zero words come from two places)
-                            const int zi = p.guH ? (gu_column(128 * ui.nb + 8 * zc, p.guH) >> 3) - 16 * ui.nb : zc;
-                            cp_async_4(smem + C::kZOff + (s * C::WP + zg) * 64 + zc * 4,
-                                       zsrc + (size_t)(j + zg) * (p.N / 8) + zi);
-                            cp_async_mbar_arrive(&wfull[s]);
-                        }
-                        __syncwarp();  // every lane's pending arrival precedes the expected-bytes arrival
                         if (lane == 0) {
                             const uint32_t bytes = (uint32_t)(n * W * 64);
                             mbar_arrive_expect_tx(&wfull[s], bytes);
@@ -298,10 +352,13 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                     }
                 }
                 wbase += (Gu + C::WP - 1) / C::WP;
+                cbase += (Gu + GB - 1) / GB;
             }
-            // drain: every stage armed must land before the CTA may exit
+            // drain: every stage and chunk armed must land before the CTA may exit
             for (int i = issued > SW ? issued - SW : 0; i < issued; ++i)
                 (void)mbar_wait(&wfull[i % SW], (i / SW) & 1, nullptr, &g_tc_status);
+            for (int i = missued > MB ? missued - MB : 0; i < missued; ++i)
+                (void)mbar_wait(&mfull[i % MB], (i / MB) & 1, nullptr, &g_tc_status);
         } else if (warp == C::kXWarp) {
             // -------------------------------------------- activation producer
             // Per activation stage (XP consecutive groups of a unit, or fewer at
@@ -397,7 +454,8 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
         const int quad = warp & 3;            // TMEM lane quadrant
         const int t = quad * 32 + lane;       // A row = tile column
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        int q = 0, wbase = 0, xbase = 0;
+        int q = 0, wbase = 0, xbase = 0, cbase = 0;
+        int cwaited = -1;  // the last metadata chunk this warp waited for
         bool ok = true;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const UnitInfo ui = unit_info(p, u);
@@ -406,8 +464,16 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
             // columns beyond a ragged tile read column W-1; their A rows only
             // feed D rows that are never written out
             const int tc = t < W ? t : W - 1;
+            // this column's zero word in a metadata chunk: box and word index
+            const int zbox = p.guH ? (tc >> 3) & 1 : tc >> 6;
+            const int zwrd = p.guH ? tc >> 4 : (tc >> 3) & 7;
             for (int j = 0; j < Gu; ++j, ++q) {
                 if ((q % C::kDeqWG) != h) continue;
+                const int ck = cbase + j / C::GB;  // metadata chunk
+                if (ck != cwaited) {
+                    if (ok && !mbar_wait_warp(&mfull[ck % C::MB], (ck / C::MB) & 1, abort_flag, &g_tc_status)) ok = false;
+                    cwaited = ck;
+                }
                 const int pw = wbase + j / C::WP, slot = j % C::WP;
                 const int s = pw % SW;
                 const bool alone = Gu - (j - slot) < C::WP;  // the stage holds this group only
@@ -421,8 +487,9 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                     const uint32_t src = smem_u32(smem + C::kPOff + s * (C::WP * 8192) + slot * W * 64);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) wq[c] = lds_v4(src + (uint32_t)((c * W + tc) * 16));
-                    const uint32_t zs = smem_u32(smem + C::kZOff + (s * C::WP + slot) * 64);
-                    const uint32_t z = (lds_u32(zs + (uint32_t)((tc >> 3) * 4)) >> (4 * (tc & 7))) & 0xFu;
+                    const uint32_t zs = smem_u32(smem + C::kMetaOff + (ck % C::MB) * C::kMetaBytes + C::kMetaScl);
+                    const uint32_t zw = lds_u32(zs + (uint32_t)(((zbox * C::GB + j % C::GB) * 8 + zwrd) * 4));
+                    const uint32_t z = (zw >> (4 * (tc & 7))) & 0xFu;
                     zz = 0x43004300u | z | (z << 16);  // bfloat16 pair (128 + z, 128 + z)
                     __syncwarp();
                     if (lane == 0) {
@@ -471,6 +538,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
             }
             wbase += (Gu + C::WP - 1) / C::WP;
             xbase += (Gu + C::XP - 1) / C::XP;
+            cbase += (Gu + C::GB - 1) / C::GB;
         }
     } else {
         if constexpr (C::kRegSplit) regs_inc<C::kRegRes>();
@@ -486,57 +554,25 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
         float2 acc[CW / 2];
 #pragma unroll
         for (int j = 0; j < CW / 2; ++j) acc[j] = make_float2(0.f, 0.f);
-        // Scales of this thread's column, kSP groups ahead: a private ring of
-        // 4-byte words (the column's fp16 scale and its neighbour's) filled by
-        // cp.async, one commit group per group of K, so that waiting for group
-        // q's word never waits for the loads issued after it.
-        uint32_t* const sring = reinterpret_cast<uint32_t*>(smem + C::kSclOff) + rt;
-        int lq_u = blockIdx.x, lq_g = -1;  // load cursor over (unit, group)
-        int lq_nb = 0, lq_g1 = 0;
-        auto issue_scale = [&](int slot) {
-            if (lq_u < p.units && (lq_g < 0 || lq_g >= lq_g1)) {  // first call or past the unit's last group
-                if (lq_g >= 0) lq_u += gridDim.x;
-                if (lq_u < p.units) {
-                    const UnitInfo ui = unit_info(p, lq_u);
-                    lq_nb = ui.nb;
-                    lq_g = ui.g0;
-                    lq_g1 = ui.g1;
-                }
-            }
-            if (lq_u < p.units) {
-                const int W = L.width(lq_nb);
-                const int tc = (t < W ? t : W - 1) & ~1;
-                const int col = 128 * lq_nb + tc;  // even: the pair (col, col + 1) is canonical-adjacent too
-                cp_async_4(sring + slot * 128 * R, p.scales + (size_t)lq_g * p.N + (p.guH ? gu_column(col, p.guH) : col));
-                ++lq_g;
-            }
-            cp_async_commit();  // possibly empty: keeps one group per slot
-        };
-        // scales are weights: with static weights the first loads go out
-        // before the preceding grid completes
-        if (p.prefetch) {
-#pragma unroll 1
-            for (int i = 0; i < C::kSP; ++i) issue_scale(i);
-            pdl_wait();
-        } else {
-            pdl_wait();
-#pragma unroll 1
-            for (int i = 0; i < C::kSP; ++i) issue_scale(i);
-        }
         // the D buffers of the first NDB groups start out free
         if (lane == 0)
             for (int i = 0; i < C::NDB; ++i) mbar_arrive(&ready[i]);
-        int q = 0;
+        int q = 0, cbase = 0;
         bool ok = true;
+        // this column's scale in a metadata chunk: box and index
+        const int sbox = p.guH ? (t >> 3) & 1 : t >> 6;
+        const int sidx = p.guH ? (t >> 4) * 8 + (t & 7) : t & 63;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const UnitInfo ui = unit_info(p, u);
             const int W = L.width(ui.nb);
-            const int odd = (t < W ? t : W - 1) & 1;  // which half of the scale word is this column's
-            for (int g = ui.g0; g < ui.g1; ++g, ++q) {
+            const int Gu = ui.g1 - ui.g0;
+            for (int j = 0; j < Gu; ++j, ++q) {
                 const int b = q % C::NDB;
-                cp_async_wait<C::kSP - 1>();  // group q's scale word has landed
-                const uint32_t sw = lds_u32(smem_u32(sring + (q % C::kSP) * 128 * R));
-                const float sc = f16_bits_to_f32((unsigned short)(odd ? sw >> 16 : sw & 0xFFFFu));
+                const int c = cbase + j / C::GB, row = j % C::GB;
+                if (row == 0 && ok && !mbar_wait_warp(&mfull[c % C::MB], (c / C::MB) & 1, abort_flag, &g_tc_status))
+                    ok = false;
+                const uint32_t sa = smem_u32(smem + C::kMetaOff + (c % C::MB) * C::kMetaBytes);
+                const float sc = f16_bits_to_f32(lds_u16(sa + (uint32_t)(((sbox * C::GB + row) * 64 + sidx) * 2)));
                 if (ok && !mbar_wait_warp(&done[q % ND], (q / ND) & 1, abort_flag, &g_tc_status)) ok = false;
                 if (ok) {
                     tc_fence_after();
@@ -575,10 +611,14 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                         if (lane == 0) mbar_arrive(&ready[(q + C::NDB) % C::kReady]);  // D buffer b free for group q + NDB
                     }
                 }
-                // the slot just read is refilled only after sc was consumed above
-                issue_scale(q % C::kSP);
+                // the chunk's last group: its buffer goes back to the producer
+                if (row == C::GB - 1 || j == Gu - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&mempty[c % C::MB]);
+                }
                 if (!ok) *abort_flag = 1;
             }
+            cbase += (Gu + C::GB - 1) / C::GB;
             // ---- end of unit: this warpgroup writes its CW tokens of the tile
             const bool all_ok = bar_and(4, 128 * R, ok && !*abort_flag);
             const int n = 128 * ui.nb + t;
@@ -676,7 +716,6 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < CW / 2; ++j) acc[j] = make_float2(0.f, 0.f);
         }
-        cp_async_wait<0>();  // the trailing commit groups are empty; nothing stays in flight
     }
 
     tc_fence_before();
@@ -775,8 +814,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 template <int NT>
-static cudaError_t launch_nt(const CUtensorMap& tm, const TcParams& prm, const TcPlan& plan, cudaStream_t s,
-                             bool pdl) {
+static cudaError_t launch_nt(const CUtensorMap& tm, const CUtensorMap& tms, const CUtensorMap& tmz, const TcParams& prm,
+                             const TcPlan& plan, cudaStream_t s, bool pdl) {
     using C = TcCfg<NT>;
     auto kern = tc_gemm_kernel<NT>;
     static int set_for[64];  // shared memory limit raised once per device
@@ -797,7 +836,7 @@ static cudaError_t launch_nt(const CUtensorMap& tm, const TcParams& prm, const T
         }
         set_for[dev] = 1;
     }
-    return launch_kernel(kern, dim3(plan.ctas), dim3(C::kThreads), plan.smem, s, pdl, tm, prm);
+    return launch_kernel(kern, dim3(plan.ctas), dim3(C::kThreads), plan.smem, s, pdl, tm, tms, tmz, prm);
 }
 
 
@@ -817,6 +856,34 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    // scales [G][N] fp16 and zero words [G][N/8]: boxes of 16 groups (the
+    // metadata chunk) x 64 columns / 8 words
+    constexpr int GB = TcCfg<16>::GB;
+    static_assert(TcCfg<16>::GB == TcCfg<192>::GB, "one chunk height for every token tile");
+    CUtensorMap tms, tmz;
+    {
+        const cuuint64_t sd[2] = {(cuuint64_t)N, (cuuint64_t)(K / 128)};
+        const cuuint64_t ss[1] = {(cuuint64_t)N * 2};
+        const cuuint32_t sb[2] = {64, GB};
+        const cuuint32_t se[2] = {1, 1};
+        r = encode(&tms, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(scales), sd, ss, sb, se,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    // zero-word rows are N/2 bytes apart: a tensor map needs that to be a multiple of 16
+    const int zmap = N % 32 == 0;
+    tmz = tms;
+    if (zmap) {
+        const cuuint64_t zd[2] = {(cuuint64_t)(N / 8), (cuuint64_t)(K / 128)};
+        const cuuint64_t zs[1] = {(cuuint64_t)N / 2};
+        const cuuint32_t zb[2] = {8, GB};
+        const cuuint32_t ze[2] = {1, 1};
+        r = encode(&tmz, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(qzeros), zd, zs, zb, ze,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
     TcParams prm;
     prm.qd = qd;
     prm.scales = scales;
@@ -837,12 +904,13 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
     const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     prm.guH = guH;
+    prm.zmap = zmap;
     switch (plan.NT) {
-        case 16: return launch_nt<16>(tm, prm, plan, s, pdl);
-        case 32: return launch_nt<32>(tm, prm, plan, s, pdl);
-        case 64: return launch_nt<64>(tm, prm, plan, s, pdl);
-        case 192: return launch_nt<192>(tm, prm, plan, s, pdl);
-        default: return launch_nt<128>(tm, prm, plan, s, pdl);
+        case 16: return launch_nt<16>(tm, tms, tmz, prm, plan, s, pdl);
+        case 32: return launch_nt<32>(tm, tms, tmz, prm, plan, s, pdl);
+        case 64: return launch_nt<64>(tm, tms, tmz, prm, plan, s, pdl);
+        case 192: return launch_nt<192>(tm, tms, tmz, prm, plan, s, pdl);
+        default: return launch_nt<128>(tm, tms, tmz, prm, plan, s, pdl);
     }
 }
 
