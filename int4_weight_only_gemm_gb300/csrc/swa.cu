@@ -29,8 +29,8 @@
 //     partials;
 //   * a second kernel (a programmatic dependent) combines the chunks of every
 //     row, out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c, one CTA per
-//     query and head group, and writes bfloat16; the partials of a call stay
-//     in L2.
+//     query and head group (a thread per head and column), and writes
+//     bfloat16; the partials of a call stay in L2.
 //
 // Every wait is bounded (common.cuh); on a timeout the kernel records
 // W4A16_ETIMEOUT, still drains its tensor-core work, frees its tensor memory
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
         const int r = threadIdx.x;                    // TMEM lane = query row
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const bool valid = r < p.R;
-        const int qi = r / p.G, hh = r - (r / p.G) * p.G;
+        const int qi = r / p.G;
         const int rq = valid ? r : 0;  // rows past R read nothing
         // q[r] into TMEM columns 0..63 as bf16 pairs (zero rows beyond R)
         {
@@ -269,26 +269,53 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
 }
 
 // Combine the chunks of the query rows of one (query, key/value head): CTA
-// (qi, hk), thread t = column t of the head, for each of the G heads of the
-// group: M = max_c m_c, out = sum_c 2^(m_c - M) O_c[t] / sum_c 2^(m_c - M) l_c.
-// Branch-free so that the loads of all chunks are in flight together.
-__global__ void __launch_bounds__(kSwaD) swa_combine_kernel(const SwaParams p) {
+// (qi, hk), thread (hh, t) = column t of head hh of the group (heads hh,
+// hh + Gb, ... when the group is wider than the block):
+// out = sum_c 2^(m_c - M) O_c[t] / sum_c 2^(m_c - M) l_c, M = max_c m_c.  The
+// chunks are read kSwaCB at a time, every load of a batch in flight together
+// (one round trip to L2 per batch), and merged with a running maximum: for up
+// to kSwaCB chunks (windows up to 1920 keys) the arithmetic is the plain
+// formula in chunk order.  Measured: the earlier form (one thread per column,
+// the group's heads in turn, the chunks' maximum and then their sums as two
+// dependent loops) took ~9 of the 19 us of a 16-token block over 1024 keys.
+constexpr int kSwaCB = 16;
+
+__global__ void __launch_bounds__(1024) swa_combine_kernel(const SwaParams p) {
     pdl_wait();  // the partials of the chunk kernel
-    const int qi = blockIdx.x, hk = blockIdx.y, t = threadIdx.x;
-    for (int hh = 0; hh < p.G; ++hh) {
+    const int qi = blockIdx.x, hk = blockIdx.y, t = threadIdx.x & 127;
+    const int Gb = (int)blockDim.x >> 7;
+    for (int hh = threadIdx.x >> 7; hh < p.G; hh += Gb) {
         const int r = qi * p.G + hh;
-        float M = -INFINITY;
-        for (int c = 0; c < p.C; ++c) M = fmaxf(M, __ldcg(p.part_ml + (((size_t)hk * p.C + c) * 128 + r) * 2));
-        float num = 0.f, den = 0.f;
-#pragma unroll 4
-        for (int c = 0; c < p.C; ++c) {
-            const size_t row = ((size_t)hk * p.C + c) * 128 + r;
-            const float mc = __ldcg(p.part_ml + row * 2);
-            const float lc = __ldcg(p.part_ml + row * 2 + 1);
-            const float oc = __ldcg(p.part_o + row * kSwaD + t);
-            const float f = mc == -INFINITY ? 0.f : exp2f(mc - M);  // no key of this row's window in chunk c
-            num = fmaf(f, oc, num);
-            den = fmaf(f, lc, den);
+        float M = -INFINITY, num = 0.f, den = 0.f;
+        for (int c0 = 0; c0 < p.C; c0 += kSwaCB) {
+            float mc[kSwaCB], lc[kSwaCB], oc[kSwaCB];
+#pragma unroll
+            for (int i = 0; i < kSwaCB; ++i) {
+                mc[i] = -INFINITY;
+                lc[i] = 0.f;
+                oc[i] = 0.f;
+                if (c0 + i < p.C) {
+                    const size_t row = ((size_t)hk * p.C + c0 + i) * 128 + r;
+                    mc[i] = __ldcg(p.part_ml + row * 2);
+                    lc[i] = __ldcg(p.part_ml + row * 2 + 1);
+                    oc[i] = __ldcg(p.part_o + row * kSwaD + t);
+                }
+            }
+            float Mb = M;
+#pragma unroll
+            for (int i = 0; i < kSwaCB; ++i) Mb = fmaxf(Mb, mc[i]);
+            if (c0 > 0) {  // the earlier batches' sums, rescaled to the new maximum
+                const float fr = M == -INFINITY ? 0.f : exp2f(M - Mb);
+                num *= fr;
+                den *= fr;
+            }
+#pragma unroll
+            for (int i = 0; i < kSwaCB; ++i) {
+                const float f = mc[i] == -INFINITY ? 0.f : exp2f(mc[i] - Mb);  // no key of this row's window in chunk c
+                num = fmaf(f, oc[i], num);
+                den = fmaf(f, lc[i], den);
+            }
+            M = Mb;
         }
         p.out[((size_t)qi * p.Hq + (size_t)hk * p.G + hh) * kSwaD + t] = f32_to_bf16_rn(num / den);
     }
@@ -388,7 +415,8 @@ cudaError_t launch_swa(const uint16_t* q, const uint16_t* kc, const uint16_t* vt
     }
     e = launch_kernel(swa_kernel, dim3(plan.C, Hkv), dim3(kSwaThreads), (size_t)kSwaSmem, s, pdl, tk, tv, prm);
     if (e != cudaSuccess) return e;
-    return launch_kernel(swa_combine_kernel, dim3(nq, Hkv), dim3(kSwaD), 0, s, true, prm);
+    const int Gb = plan.G < 8 ? plan.G : 8;  // heads of the group a combine CTA holds at once
+    return launch_kernel(swa_combine_kernel, dim3(nq, Hkv), dim3(kSwaD * Gb), 0, s, true, prm);
 }
 
 int swa_read_status() {
