@@ -46,8 +46,11 @@
  *   - y must not overlap any input.  Calls are thread-safe when they use
  *     different workspaces; two calls that may run at the same time on the
  *     GPU must not share one workspace.
- *   - Requirements: M >= 1, N >= 8, N % 8 == 0, K >= 128, K % 128 == 0,
- *     group == 128; M, N, K < 2^31 and K*N/8 < 2^31.
+ *   - Requirements: M >= 0, N >= 8, N % 8 == 0, K >= 128, K % 128 == 0,
+ *     group == 128; M, N, K < 2^31 and K*N/8 < 2^31.  M == 0 (an empty
+ *     batch) computes nothing: after the checks of group, N, K (and the
+ *     flags) the call returns W4A16_OK without reading any pointer or
+ *     launching.
  */
 #ifndef W4A16_H
 #define W4A16_H
@@ -74,9 +77,11 @@ typedef enum {
 } w4a16_status;
 
 /*
- * Kernel choice for w4a16_gemm_path.  AUTO picks from times measured on
- * GB300: the GEMV when M <= 2, or M <= 4 with K*N <= 16M weights (and its
- * activation copy fits in shared memory); the tensor-core GEMM otherwise.
+ * Kernel choice for w4a16_gemm_path.  AUTO looks the problem up in a table
+ * generated from times measured on GB300 (every candidate kernel over the
+ * decoder's shapes at M = 1 .. 8192), keyed by the weight count K*N (up to
+ * 16M, up to 64M, above) and an M bucket: one of the two GEMV forms for small
+ * M where it fits, the tensor-core GEMM with the table's token tile otherwise.
  */
 typedef enum {
     W4A16_PATH_AUTO = 0,

@@ -126,8 +126,9 @@ constexpr unsigned kKnownFlags = W4A16_FLAG_PDL | W4A16_FLAG_STATIC_WEIGHTS | W4
 int run_gemm(int path, unsigned flags, const void* x, const uint32_t* qd, const void* scales, const uint32_t* qzeros,
              int M, int N, int K, int group, void* y, void* ws, size_t ws_bytes, cudaStream_t stream, int guH = 0) {
     if (flags & ~kKnownFlags) return W4A16_EINVAL;
+    if (path < W4A16_PATH_AUTO || path > W4A16_PATH_GEMV_CS) return W4A16_EINVAL;
     int st = check_gemm(x, qd, scales, qzeros, M, N, K, group, y, guH ? guH : N);
-    if (st != W4A16_OK) return st;
+    if (st != W4A16_OK || M == 0) return st;  // M == 0: nothing to compute
     const int dev = current_device();
     if (dev < 0) return W4A16_ECUDA;
     const int sms = device_sms(dev);
@@ -169,8 +170,12 @@ int run_gemm(int path, unsigned flags, const void* x, const uint32_t* qd, const 
 // ny: columns of y (N for the plain product, N / 2 for the fused gate/up one)
 int check_gemm(const void* x, const uint32_t* qd, const void* scales, const uint32_t* qzeros, int M, int N, int K,
                int group, void* y, int ny) {
+    if (M < 0) return W4A16_EINVAL;
+    if (M == 0) {  // an empty batch: only the shape is checked, no pointer is read
+        if (group != 128) return W4A16_EUNSUPPORTED;
+        return check_kn(N, K);
+    }
     if (!x || !qd || !scales || !qzeros || !y) return W4A16_EINVAL;
-    if (M < 1) return W4A16_EINVAL;
     if (group != 128) return W4A16_EUNSUPPORTED;
     int st = check_kn(N, K);
     if (st != W4A16_OK) return st;

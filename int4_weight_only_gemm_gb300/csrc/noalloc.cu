@@ -59,7 +59,7 @@ extern "C" int w4a16_gemm_noalloc(const void* x, const uint32_t* qweight_dev, co
                                   w4a16_stream_t stream) {
     // the same argument rules as w4a16_gemm
     const int chk = check_gemm(x, qweight_dev, scales, qzeros, M, N, K, group, y, N);
-    if (chk != W4A16_OK) return chk;
+    if (chk != W4A16_OK || M == 0) return chk;  // M == 0: nothing to compute
     if (M > 8) return W4A16_EUNSUPPORTED;  // only the GEMV has a no-allocation form
 
     int dev = -1;

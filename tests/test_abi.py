@@ -65,7 +65,7 @@ def test_host_validation_rejects_before_launch(lib):
     assert _gemm(lib, None, B, C, D, 1, 128, 256, 128, E) == -1
     assert _gemm(lib, A, B, C, D, 1, 128, 256, 128, None) == -1
     # bad sizes
-    assert _gemm(lib, A, B, C, D, 0, 128, 256, 128, E) == -1
+    assert _gemm(lib, A, B, C, D, -1, 128, 256, 128, E) == -1
     assert _gemm(lib, A, B, C, D, 1, 12, 256, 128, E) == -1       # N % 8
     assert _gemm(lib, A, B, C, D, 1, 0, 256, 128, E) == -1
     # unsupported group / K
@@ -77,6 +77,28 @@ def test_host_validation_rejects_before_launch(lib):
     assert _gemm(lib, A, B, C, D, 1, 128, 256, 128, E + 8) == -2
     # output overlapping an input
     assert _gemm(lib, A, B, C, D, 1, 128, 256, 128, A + 256) == -1
+
+
+def test_empty_batch_is_a_checked_no_op(lib):
+    """M == 0 computes nothing: the shape is still checked, no pointer is read
+    (null pointers pass), and the call returns before any CUDA call -- which
+    is why it succeeds here, without a GPU."""
+    assert _gemm(lib, None, None, None, None, 0, 128, 256, 128, None) == 0
+    assert _gemm(lib, None, None, None, None, 0, 12, 256, 128, None) == -1   # N % 8
+    assert _gemm(lib, None, None, None, None, 0, 128, 320, 128, None) == -3  # K % 128
+    assert _gemm(lib, None, None, None, None, 0, 128, 256, 64, None) == -3   # group
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    lib.w4a16_gemm_ex.argtypes = [i, ctypes.c_uint, vp, vp, vp, vp, i, i, i, i, vp, vp, ctypes.c_size_t, vp]
+    assert lib.w4a16_gemm_ex(0, 0, None, None, None, None, 0, 128, 256, 128, None, None, 0, None) == 0
+    assert lib.w4a16_gemm_ex(9, 0, None, None, None, None, 0, 128, 256, 128, None, None, 0, None) == -1  # path
+    assert lib.w4a16_gemm_ex(0, 1 << 30, None, None, None, None, 0, 128, 256, 128, None, None, 0, None) == -1  # flags
+    lib.w4a16_gemm_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, vp, vp]
+    assert lib.w4a16_gemm_noalloc(None, None, None, None, 0, 128, 256, 128, None, None) == 0
+    lib.w4a16_gemm_gate_up_silu.argtypes = [i, ctypes.c_uint, vp, vp, vp, vp, i, i, i, i, vp, vp, ctypes.c_size_t, vp]
+    assert lib.w4a16_gemm_gate_up_silu(0, 0, None, None, None, None, 0, 64, 256, 128, None, None, 0, None) == 0
+    lib.w4a16_workspace_bytes.restype = ctypes.c_size_t
+    lib.w4a16_workspace_bytes.argtypes = [i, i, i, i]
+    assert lib.w4a16_workspace_bytes(0, 128, 256, 128) == 0
 
 
 def test_pack_validation(lib):

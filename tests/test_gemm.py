@@ -183,6 +183,19 @@ def test_exact_case_bit_exact(M):
         assert np.array_equal(got, want), f"path {path}: {np.count_nonzero(got != want)} bits differ"
 
 
+@pytest.mark.parametrize("path", [AUTO, TC, SPLITK, CS])
+def test_empty_batch_launches_nothing(path):
+    """M = 0 (an empty batch): an empty result, no kernel launched."""
+    import int4_weight_only_gemm_gb300 as w
+    d = Device(wi.generate_named("qkv", 1, 0))
+    x0 = torch.empty((0, d.prob.K), dtype=torch.bfloat16, device="cuda")
+    before = w.w4a16_launch_count()
+    y = d.run(path, x=x0)
+    torch.cuda.synchronize()
+    assert tuple(y.shape) == (0, d.prob.N)
+    assert w.w4a16_launch_count() == before
+
+
 def test_zero_codes_give_zero():
     K, N, M = 512, 256, 4
     r = np.random.default_rng(1)

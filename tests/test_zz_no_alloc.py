@@ -101,5 +101,6 @@ def test_noalloc_rejects_what_it_cannot_run():
     n0 = w.w4a16_launch_count()
     assert _noalloc(lib, d, 9, y) == w.W4A16_EUNSUPPORTED  # beyond the GEMV's M
     assert lib.w4a16_gemm_noalloc(None, None, None, None, 1, 128, 256, 128, None, None) == w.W4A16_EINVAL
-    assert _noalloc(lib, d, 0, y) == w.W4A16_EINVAL
+    assert _noalloc(lib, d, -1, y) == w.W4A16_EINVAL
+    assert _noalloc(lib, d, 0, y) == w.W4A16_OK  # an empty batch: nothing to compute
     assert w.w4a16_launch_count() == n0
