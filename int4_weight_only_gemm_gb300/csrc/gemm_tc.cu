@@ -729,11 +729,11 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// Token tile when neither the caller nor the dispatch table names one.  An
-// MMA of N <= 128 takes about as long as one of N = 128 (~47 ns for M = 128,
-// K = 16, measured), while N = 256 runs at the full rate, so large M takes
-// 192-token tiles: two D buffers of 192 columns still fit beside two A
-// buffers in the 512 tensor-memory columns.
+// Token tile when neither the caller nor the dispatch table names one (the
+// table's measured choices follow the same steps): the smallest tile that
+// holds M up to 64 tokens, 128 up to 256, then 192 -- two D buffers of 192
+// columns still fit beside two A buffers in the 512 tensor-memory columns, and
+// the larger tile reads each weight slab for more tokens.
 static int tc_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 256 ? 128 : 192; }
 
 bool tc_plan(int M, int N, int K, int sms, TcPlan* out, int force_nt) {
