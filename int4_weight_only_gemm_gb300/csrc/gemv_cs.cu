@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kCsThreads, MT <= 2 ? 2 : 1) gemv_cs_kernel(co
     // is uint4 512 KB nb + W r + (n % 128) of the device layout (W = width of
     // tile nb), so a column's items are W uint4 apart.
     const uint4* lptr = nullptr;
-    int lstride = 0, lp = 0, lr = 0, issued = 0;
+    int lstride = 0, lp = 0, lr = 0, issued = 0, lslot = 0;
     auto set_column = [&](int pass) {
         const int n = c0 + j0 + pass * kCsThreads;
         const int nb = n >> 7;
@@ -127,7 +127,8 @@ __global__ void __launch_bounds__(kCsThreads, MT <= 2 ? 2 : 1) gemv_cs_kernel(co
     // item `issued` into its slot, one commit group per item (possibly empty)
     auto copy_next = [&]() {
         if (issued < nitems) {
-            cp_async_16(ring + (size_t)(issued % (D + 1)) * kCsThreads, lptr);
+            cp_async_16(ring + (size_t)lslot * kCsThreads, lptr);
+            lslot = lslot == D ? 0 : lslot + 1;
             lptr += lstride;
             if (++lr == nr) {
                 lr = 0;
@@ -198,8 +199,8 @@ __global__ void __launch_bounds__(kCsThreads, MT <= 2 ? 2 : 1) gemv_cs_kernel(co
     const uint32_t xs_a = smem_u32(xs);
     const uint32_t ring_a = smem_u32(ring);
     const uint32_t xrow = (uint32_t)p.K * 2;  // bytes between token rows of xs
-    constexpr int NCH = MT == 1 ? 4 : 2;      // independent chains a token
-    int k = 0;                                // item being multiplied
+    constexpr int NCH = MT == 1 ? 4 : 2;  // independent chains a token
+    int kslot = 0;                        // ring slot of the item being multiplied
 #pragma unroll 1
     for (int pass = 0; pass < npass; ++pass) {
         const int jj = j0 + pass * kCsThreads;
@@ -215,10 +216,11 @@ __global__ void __launch_bounds__(kCsThreads, MT <= 2 ? 2 : 1) gemv_cs_kernel(co
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) d[m][c] = 0.f;
 #pragma unroll
-            for (int it = 0; it < 4; ++it, ++k) {  // the group's four items
-                cp_async_wait<D - 1>();            // item k has landed (D - 1 newer copies may be pending)
-                const uint4 w = lds_v4(ring_a + (uint32_t)(k % (D + 1)) * (kCsThreads * 16));
-                copy_next();                       // item k + D, into the slot item k - 1 used
+            for (int it = 0; it < 4; ++it) {  // the group's four items
+                cp_async_wait<D - 1>();  // this item has landed (D - 1 newer copies may be pending)
+                const uint4 w = lds_v4(ring_a + (uint32_t)kslot * (kCsThreads * 16));
+                kslot = kslot == D ? 0 : kslot + 1;
+                copy_next();  // the item D further on, into the slot the previous item used
                 const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
                 const int r = 4 * g + it;
 #pragma unroll
@@ -242,9 +244,12 @@ __global__ void __launch_bounds__(kCsThreads, MT <= 2 ? 2 : 1) gemv_cs_kernel(co
             const float zoff = 128.f + (float)((szw[g * (C >> 2) + (jj >> 2)] >> zsh) & 0xFu);
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                float dot = d[m][0];
+                // pairwise sum of the chains
 #pragma unroll
-                for (int c = 1; c < NCH; ++c) dot += d[m][c];
+                for (int w2 = 1; w2 < NCH; w2 *= 2)
+#pragma unroll
+                    for (int c = 0; c + w2 < NCH; c += 2 * w2) d[m][c] += d[m][c + w2];
+                const float dot = d[m][0];
                 acc[m] = fmaf(sc, fmaf(-zoff, xsum[m * G + g], dot), acc[m]);
             }
         }
