@@ -214,6 +214,8 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
     constexpr int SA = C::SA;
     constexpr int R = C::R;
     constexpr int ND = C::kDone;
+    // the last unit's split-tile reduction is run by the whole CTA
+    constexpr bool kDeferSplit = R == 1 && !C::kRegSplit;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -231,6 +233,8 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     int* sh_last = const_cast<int*>(abort_flag) + 1;
+    // a split tile whose reduction waits for the whole CTA: flag, tile, pieces, first token, column tile
+    int* sh_defer = sh_last + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -251,6 +255,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
         else if (i == nb) {
             mbar_init(mma_done, C::kMmaIssuers);
             *abort_flag = 0;
+            sh_defer[0] = 0;
         }
         if (i <= nb) fence_mbar_init();
     }
@@ -648,12 +653,15 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                     }
                 } else {
                     const int tile = ui.ptile;  // counters and partials of the split tiles only
-                    // partial sums: [split tile][piece][NT tokens][128 columns], so that a
-                    // warp writes (and the reduction reads) 32 adjacent columns at once;
-                    // this warpgroup's CW tokens
-                    float* part = p.partials + (((size_t)tile * ui.ns + ui.split) * NT + r * CW) * 128 + t;
+                    // partial sums: [split tile][piece][NT / 4][128 columns][4 tokens]: a
+                    // thread writes (and the reduction reads) four tokens of its column
+                    // as one 16-byte vector, a warp 512 contiguous bytes
+                    float4* part = reinterpret_cast<float4*>(p.partials) +
+                                   (((size_t)tile * ui.ns + ui.split) * (NT / 4) + r * (CW / 4)) * 128 + t;
 #pragma unroll
-                    for (int j = 0; j < CW; ++j) part[(size_t)j * 128] = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
+                    for (int j = 0; j < CW / 4; ++j)
+                        part[(size_t)j * 128] =
+                            make_float4(acc[2 * j].x, acc[2 * j].y, acc[2 * j + 1].x, acc[2 * j + 1].y);
                     // hand-off: the barrier orders the warpgroups' partial stores
                     // before one thread, whose gpu-scope fence publishes them
                     // with its arrival; the last arrival fences again before
@@ -667,24 +675,43 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                         *sh_last = last;
                     }
                     asm volatile("bar.sync 5, %0;" ::"r"(128 * R) : "memory");
-                    if (*sh_last) {
+                    // Only with one rescale warpgroup (NT <= 32), where its own
+                    // reduction needs the most round trips per element; never with
+                    // the register split, where every warp would run it, also those
+                    // that gave registers away.
+                    const bool last_unit = kDeferSplit && u + (int)gridDim.x >= p.units;
+                    if (*sh_last && last_unit) {
+                        // the CTA's last unit: every warp of the CTA joins the
+                        // reduction once the roles are done (more loads in flight)
+                        if (rt == 0) {
+                            sh_defer[1] = tile;
+                            sh_defer[2] = ui.ns;
+                            sh_defer[3] = ui.mb * NT;
+                            sh_defer[4] = ui.nb;
+                            sh_defer[0] = 1;
+                        }
+                    } else if (*sh_last) {
                         // every split's values for this thread, summed in split order,
                         // 16 tokens at a time
-                        const float* base = p.partials + ((size_t)tile * ui.ns * NT + r * CW) * 128 + t;
-                        const size_t sstride = (size_t)128 * NT;  // floats between splits
+                        const float4* base = reinterpret_cast<const float4*>(p.partials) +
+                                             ((size_t)tile * ui.ns * (NT / 4) + r * (CW / 4)) * 128 + t;
+                        const size_t sstride = (size_t)(NT / 4) * 128;  // float4s between splits
 #pragma unroll 1
                         for (int j0 = 0; j0 < CW; j0 += 16) {
-                            float sv[16];
+                            float4 sum[4];
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) sv[j] = 0.f;
+                            for (int i = 0; i < 4; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 2
                             for (int sp = 0; sp < ui.ns; ++sp) {
 #pragma unroll
-                                for (int j = 0; j < 16; ++j) sv[j] += __ldcg(base + sp * sstride + (size_t)(j0 + j) * 128);
+                                for (int i = 0; i < 4; ++i) {
+                                    const float4 v = __ldcg(base + sp * sstride + (size_t)(j0 / 4 + i) * 128);
+                                    sum[i].x += v.x;
+                                    sum[i].y += v.y;
+                                    sum[i].z += v.z;
+                                    sum[i].w += v.w;
+                                }
                             }
-                            const float4 sum[4] = {make_float4(sv[0], sv[1], sv[2], sv[3]), make_float4(sv[4], sv[5], sv[6], sv[7]),
-                                                   make_float4(sv[8], sv[9], sv[10], sv[11]),
-                                                   make_float4(sv[12], sv[13], sv[14], sv[15])};
                             if (p.guH) {
                                 const bool gate = !(t & 8);
                                 const size_t col = (size_t)gu_column(gate ? n : n - 8, p.guH);
@@ -723,6 +750,69 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
     if (warp == C::kProdWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
+    }
+    if constexpr (kDeferSplit) {
+    if (sh_defer[0] && !*abort_flag) {
+        // Deferred reduction of a split tile by every thread of the CTA: element
+        // e of a piece's partials ([NT / 4][128 columns][4 tokens]) is summed
+        // over the pieces in piece order, the loads of up to kE elements and
+        // kS pieces in flight at once.
+        constexpr int kE = 3, kS = 8;
+        const int tile = sh_defer[1], ns = sh_defer[2], tokb = sh_defer[3], nbt = sh_defer[4];
+        const int W = L.width(nbt);
+        const float* base = p.partials + (size_t)tile * ns * NT * 128;
+        const int nthr = (int)blockDim.x;
+        const int nel = p.guH ? NT * 64 : NT * 128;  // gate/up: one element per gate column
+        for (int e0 = (int)threadIdx.x; e0 < nel; e0 += kE * nthr) {
+            int ea[kE];
+            float sum[kE], sup[kE];
+#pragma unroll
+            for (int k = 0; k < kE; ++k) {
+                const int i = e0 + k * nthr;
+                if (p.guH) {  // i -> (token quad, gate column with bit 3 clear, token)
+                    const int jj = i % 4, rc = i / 4, tq = rc / 64, c64 = rc % 64;
+                    ea[k] = i < nel ? (tq * 128 + (c64 / 8) * 16 + (c64 % 8)) * 4 + jj : -1;
+                } else {
+                    ea[k] = i < nel ? i : -1;
+                }
+                sum[k] = 0.f;
+                sup[k] = 0.f;
+            }
+            for (int sp0 = 0; sp0 < ns; sp0 += kS) {
+                float v[kE][kS], vu[kE][kS];
+#pragma unroll
+                for (int k = 0; k < kE; ++k)
+#pragma unroll
+                    for (int q2 = 0; q2 < kS; ++q2) {
+                        const bool in = ea[k] >= 0 && sp0 + q2 < ns;
+                        const float* pp = base + (size_t)(sp0 + q2) * NT * 128 + ea[k];
+                        v[k][q2] = in ? __ldcg(pp) : 0.f;
+                        vu[k][q2] = in && p.guH ? __ldcg(pp + 8 * 4) : 0.f;
+                    }
+#pragma unroll
+                for (int k = 0; k < kE; ++k)
+#pragma unroll
+                    for (int q2 = 0; q2 < kS; ++q2)
+                        if (sp0 + q2 < ns) {
+                            sum[k] += v[k][q2];
+                            sup[k] += vu[k][q2];
+                        }
+            }
+#pragma unroll
+            for (int k = 0; k < kE; ++k) {
+                if (ea[k] < 0) continue;
+                const int col = (ea[k] / 4) % 128;
+                const int tok = tokb + (ea[k] / 512) * 4 + ea[k] % 4;
+                if (tok >= p.M) continue;
+                const int n = 128 * nbt + col;
+                if (p.guH)
+                    p.y[(size_t)tok * p.guH + gu_column(n, p.guH)] = f32_to_bf16_rn(silu_mul(sum[k], sup[k]));
+                else if (col < W)
+                    p.y[(size_t)tok * p.N + n] = f32_to_bf16_rn(sum[k]);
+            }
+        }
+        if (threadIdx.x == 0) p.counters[tile] = 0u;
+    }
     }
 }
 

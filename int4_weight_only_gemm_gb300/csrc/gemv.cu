@@ -268,20 +268,36 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     // loaded two units ahead of use: (sc0, zw0) for unit i, (sc1, zw1) for i + 4
     int pv = ub + wg;  // next unit to fetch
     int pnb = pv / p.KB, pkb = pv - pnb * p.KB;
+    // the column's scale and zero-word pointers at group pkb of tile pnb; four
+    // units on they move four groups down, unless the unit is in a later tile
+    const uint16_t* sp = nullptr;
+    const uint32_t* zp = nullptr;
+    auto aim = [&]() {
+        const int Wp = L.width(pnb);
+        const int tp = t < Wp ? t : Wp - 1;
+        const int n = 128 * pnb + tp;
+        const int cn = p.guH ? gu_column(n, p.guH) : n;  // canonical column of the scale and zero
+        sp = p.scales + (size_t)pkb * p.N + cn;
+        zp = p.qzeros + (size_t)pkb * (p.N / 8) + (cn >> 3);
+    };
+    if (pv < ue) aim();
+    const size_t sstep = (size_t)4 * p.N, zstep = (size_t)p.N / 2;
     auto fetch = [&](uint16_t& sc, uint32_t& zw) {
         if (pv < ue) {
-            const int Wp = L.width(pnb);
-            const int tp = t < Wp ? t : Wp - 1;
-            const int n = 128 * pnb + tp;
-            const int cn = p.guH ? gu_column(n, p.guH) : n;  // canonical column of the scale and zero
-            sc = __ldg(p.scales + (size_t)pkb * p.N + cn);
-            zw = __ldg(p.qzeros + (size_t)pkb * (p.N / 8) + (cn >> 3));
+            sc = __ldg(sp);
+            zw = __ldg(zp);
         }
         pv += 4;
         pkb += 4;
-        while (pkb >= p.KB) {
-            pkb -= p.KB;
-            ++pnb;
+        if (pkb < p.KB) {
+            sp += sstep;
+            zp += zstep;
+        } else {
+            do {
+                pkb -= p.KB;
+                ++pnb;
+            } while (pkb >= p.KB);
+            if (pv < ue) aim();
         }
     };
     uint16_t sc0 = 0, sc1 = 0;

@@ -86,8 +86,12 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
     const int t = threadIdx.x;
     const int b = blockIdx.x;
     const int P = (int)gridDim.x;
-    const int c0 = p.unit * (int)((long long)b * p.U / P);
-    const int c1 = p.unit * (int)((long long)(b + 1) * p.U / P);
+    // slice bounds: 32-bit arithmetic where the products fit (a 64-bit
+    // division costs tens of instructions, paid by every thread)
+    const bool narrow = p.U < (1 << 22) && p.KB < (1 << 22);
+    const int c0 = p.unit * (narrow ? (int)((unsigned)b * (unsigned)p.U / (unsigned)P) : (int)((long long)b * p.U / P));
+    const int c1 = p.unit * (narrow ? (int)((unsigned)(b + 1) * (unsigned)p.U / (unsigned)P)
+                                    : (int)((long long)(b + 1) * p.U / P));
     const int C = c1 - c0;
     const int G = p.KB;
     const int S = cs_ranges(C, G);
@@ -106,7 +110,8 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
     const bool active = t < S * C || S == 1;
     const int j0 = S == 1 ? t : t % C;
     const int s = S == 1 ? 0 : t / C;
-    const int g0 = (int)((long long)s * G / S), g1 = (int)((long long)(s + 1) * G / S);
+    const int g0 = narrow ? (int)((unsigned)s * (unsigned)G / (unsigned)S) : (int)((long long)s * G / S);
+    const int g1 = narrow ? (int)((unsigned)(s + 1) * (unsigned)G / (unsigned)S) : (int)((long long)(s + 1) * G / S);
     const int nr = 4 * (g1 - g0);  // items of one column
     const int npass = S == 1 ? (j0 < C ? (C - j0 + kCsThreads - 1) / kCsThreads : 0) : (active ? 1 : 0);
     const int nitems = npass * nr;
@@ -124,12 +129,13 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
         lptr = qd4 + (size_t)512 * p.KB * nb + (size_t)lstride * (4 * g0) + (n & 127);
     };
     // item `issued` into its slot, one commit group per item (possibly empty)
+    const bool passes = npass > 1;  // a thread with one column needs no column switch
     auto copy_next = [&]() {
         if (issued < nitems) {
             cp_async_16(ring + (size_t)lslot * kCsThreads, lptr);
             lslot = lslot == D ? 0 : lslot + 1;
             lptr += lstride;
-            if (++lr == nr) {
+            if (passes && ++lr == nr) {
                 lr = 0;
                 if (++lp < npass) set_column(lp);
             }
@@ -158,17 +164,8 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
         for (int i = 0; i < D; ++i) copy_next();
     };
 
-    if (p.prefetch) {
-        start_items();
-        stage_scales_zeros();
-    }
-    pdl_wait();  // x, and y below, only after the preceding grid
-    if (!p.prefetch) {
-        start_items();
-        stage_scales_zeros();
-    }
-    {
-        // activations: rows m < M copied (asynchronously), rows M..MT-1 zero
+    // activations: rows m < M copied (asynchronously), rows M..MT-1 zero
+    auto copy_x = [&]() {
         const int n16 = MT * p.K / 8;
         const int v16 = p.M * p.K / 8;
         const uint4* xg = reinterpret_cast<const uint4*>(p.x);
@@ -178,7 +175,24 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
             else xv[i] = make_uint4(0, 0, 0, 0);
         }
         cp_async_commit();
-        cp_async_wait<0>();  // the first D items, the scales and zeros, and x
+    };
+    // Commit groups complete in order.  With static weights the first D items
+    // and the scales go out before the grid dependency resolves and x after
+    // it, so x's group is the newest and all must have landed; otherwise x
+    // and the scales go first, and the multiplication starts once they and
+    // the first item are in, while the other D - 1 items are still coming.
+    if (p.prefetch) {
+        start_items();
+        stage_scales_zeros();
+        pdl_wait();  // x, and y below, only after the preceding grid
+        copy_x();
+        cp_async_wait<0>();
+    } else {
+        pdl_wait();
+        copy_x();
+        stage_scales_zeros();
+        start_items();
+        cp_async_wait<D>();  // x and the scales (the D item groups may be pending)
     }
     __syncthreads();
     // per-group activation sums, one (token, group) per warp
