@@ -73,17 +73,14 @@ int repack_gate_up(bool pack, const uint32_t* src, uint32_t* dst, int K, int H, 
     return W4A16_OK;
 }
 
-// The column-sliced GEMV gives every CTA whole columns: no split-K hand-off,
-// which dominates small matrices, but its register-ring stream is slower than
-// the split-K form's bulk copies once a CTA has much to read (measured on the
-// decoder's shapes at M = 1: 4.4 / 4.6 us against 5.4 / 5.6 us for qkv and
-// o_proj, 36 KB a CTA; 14.4 / 9.8 us against 9.0 / 7.5 us for gate_up and
-// down, 170 and 85 KB a CTA).  It is the GEMV's form when every SM gets a
-// slice of at most 64 KB of packed weights.
-constexpr long long kCsMaxCtaBytes = 64 << 10;
+// The column-sliced GEMV gives every CTA whole columns: no split-K hand-off.
+// Measured on the decoder's shapes and the vocabulary head at M = 1, 2, 4, 8
+// it is as fast as the split-K form or faster (at M = 1: qkv 4.1 against
+// 5.5 us, down 6.7 against 7.4, gate_up 8.2 against 8.2, vocabulary 46 against
+// 49), provided its slices fill the GPU; with fewer columns than that the
+// split-K form spreads K over the idle SMs.
 bool gemv_uses_cs(int M, int N, int K, int sms, int guH, GemvCsPlan* cp) {
-    return gemv_cs_plan(M, N, K, sms, guH, cp) && cp->ctas >= sms &&
-           (long long)K * N / 2 <= kCsMaxCtaBytes * cp->ctas;
+    return gemv_cs_plan(M, N, K, sms, guH, cp) && cp->ctas >= sms;
 }
 
 // Kernel choice for AUTO: the dispatch table's row (measured on GB300 over
