@@ -234,12 +234,16 @@ class Workload:
             p = wi.generate_named(shape, M, seed)
             x, qw, sc, qz = w.to_device(p, device)
             qd = w.w4a16_pack(qw)
+            # every copy has its own weights, scales and zero points, so that
+            # all three stream from HBM as they would for distinct layers
             qds = [qd] + [qd.clone() for _ in range(copies - 1)]
+            scs = [sc] + [sc.clone() for _ in range(copies - 1)]
+            qzs = [qz] + [qz.clone() for _ in range(copies - 1)]
             del qw
             y = torch.empty((M, p.N), dtype=torch.bfloat16, device=device)
             need = w.w4a16_workspace_bytes_max(M, p.N, p.K)  # any path or token tile
             ws = w.new_workspace(need, device)
-            self.gemms.append(dict(p=p, shape=shape, M=M, K=p.K, N=p.N, x=x, qds=qds, sc=sc, qz=qz, y=y, ws=ws,
+            self.gemms.append(dict(p=p, shape=shape, M=M, K=p.K, N=p.N, x=x, qds=qds, scs=scs, qzs=qzs, y=y, ws=ws,
                                    ws_bytes=ws.numel()))
         self.copies = copies
         self.bytes = sum(gemm_bytes(g["M"], g["K"], g["N"]) for g in self.gemms)
@@ -251,8 +255,8 @@ class Workload:
         for i, g in enumerate(self.gemms):
             if only is not None and i != only:
                 continue
-            st = w.w4a16_gemm_raw(g["x"].data_ptr(), g["qds"][copy].data_ptr(), g["sc"].data_ptr(),
-                                  g["qz"].data_ptr(), g["M"], g["N"], g["K"], 128, g["y"].data_ptr(),
+            st = w.w4a16_gemm_raw(g["x"].data_ptr(), g["qds"][copy].data_ptr(), g["scs"][copy].data_ptr(),
+                                  g["qzs"][copy].data_ptr(), g["M"], g["N"], g["K"], 128, g["y"].data_ptr(),
                                   g["ws"].data_ptr(), g["ws_bytes"], path, stream_ptr, flags)
             if st != 0:
                 raise RuntimeError(f"w4a16_gemm failed: {w.w4a16_status_str(st)}")
@@ -347,7 +351,7 @@ def measure_e2e(w, torch, wl, steps):
         c = i % wl.copies
         dx.copy_(hx, non_blocking=True)
         for j, g in enumerate(wl.gemms):
-            w.w4a16_gemm(dxs[j], g["qds"][c], g["sc"], g["qz"], out=dys[j], workspace=g["ws"])
+            w.w4a16_gemm(dxs[j], g["qds"][c], g["scs"][c], g["qzs"][c], out=dys[j], workspace=g["ws"])
         hy.copy_(dy, non_blocking=True)
         stream.synchronize()
 
@@ -427,25 +431,27 @@ def measure_gate_up_silu(w, torch, device, hbm, bf16_peak):
         x, qw, sc, qz = w.to_device(p, device)
         fused = [w.w4a16_pack_gate_up(qw) for _ in range(copies)]
         plain = [w.w4a16_pack(qw) for _ in range(copies)]
+        scs = [sc] + [sc.clone() for _ in range(copies - 1)]
+        qzs = [qz] + [qz.clone() for _ in range(copies - 1)]
         del qw
         ws = w.new_workspace(w.w4a16_workspace_bytes(M, N, K), device)
         y_f = torch.empty((M, H), dtype=torch.bfloat16, device=device)
         y_p = torch.empty((M, N), dtype=torch.bfloat16, device=device)
         res = {}
         for name, qds, call in (
-                ("fused", fused, lambda qd: w.w4a16_gemm_gate_up_silu(x, qd, sc, qz, out=y_f, workspace=ws)),
-                ("plain", plain, lambda qd: w.w4a16_gemm(x, qd, sc, qz, out=y_p, workspace=ws))):
+                ("fused", fused, lambda c: w.w4a16_gemm_gate_up_silu(x, fused[c], scs[c], qzs[c], out=y_f, workspace=ws)),
+                ("plain", plain, lambda c: w.w4a16_gemm(x, plain[c], scs[c], qzs[c], out=y_p, workspace=ws))):
             s = torch.cuda.Stream()
             s.wait_stream(torch.cuda.current_stream())
             with torch.cuda.stream(s):
-                for qd in qds:
-                    call(qd)
+                for c in range(len(qds)):
+                    call(c)
             torch.cuda.current_stream().wait_stream(s)
             torch.cuda.synchronize()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                for qd in qds:
-                    call(qd)
+                for c in range(len(qds)):
+                    call(c)
             for _ in range(3):
                 g.replay()
             torch.cuda.synchronize()
@@ -513,16 +519,18 @@ def time_gemm(w, torch, p, device, path, flags, reps_target_ms=20.0):
     x, qw, sc, qz = w.to_device(p, device)
     qd = w.w4a16_pack(qw)
     del qw
-    wbytes = p.K * p.N // 2
+    wbytes = gemm_bytes(p.M, p.K, p.N)
     copies = int(min(64, max(2, -(-int(2.1 * L2_BYTES) // wbytes))))
     qds = [qd] + [qd.clone() for _ in range(copies - 1)]
+    scs = [sc] + [sc.clone() for _ in range(copies - 1)]
+    qzs = [qz] + [qz.clone() for _ in range(copies - 1)]
     y = torch.empty((p.M, p.N), dtype=torch.bfloat16, device=device)
     ws = w.new_workspace(w.w4a16_workspace_bytes_max(p.M, p.N, p.K), device)
     nbytes = ws.numel()
 
     def launch_all(stream_ptr):
-        for q in qds:
-            st = w.w4a16_gemm_raw(x.data_ptr(), q.data_ptr(), sc.data_ptr(), qz.data_ptr(), p.M, p.N, p.K, 128,
+        for q, sq, zq in zip(qds, scs, qzs):
+            st = w.w4a16_gemm_raw(x.data_ptr(), q.data_ptr(), sq.data_ptr(), zq.data_ptr(), p.M, p.N, p.K, 128,
                                   y.data_ptr(), ws.data_ptr(), nbytes, path, stream_ptr, flags)
             if st != 0:
                 raise RuntimeError(f"w4a16_gemm path {path} flags {flags}: {w.w4a16_status_str(st)}")
@@ -551,7 +559,7 @@ def time_gemm(w, torch, p, device, path, flags, reps_target_ms=20.0):
     e1.record()
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / (reps * copies)
-    del g, qds, qd, x, y, ws
+    del g, qds, scs, qzs, qd, x, y, ws
     return us, copies
 
 
@@ -600,8 +608,8 @@ def tune_dispatch(path_out, ms=TUNE_M):
             entries.append({"shape": shape, "K": p.K, "N": p.N, "M": M, "config": name, "us": round(us, 3)})
             print(json.dumps(entries[-1]), flush=True)
         torch.cuda.empty_cache()
-    doc = {"what": "microseconds per launch of each dispatch candidate (CUDA graphs over rotating weight copies "
-                   "> 2x L2); written by bench.py --tune-dispatch",
+    doc = {"what": "microseconds per launch of each dispatch candidate (CUDA graphs over rotating copies of the "
+                   "weights, scales and zero points, > 2x L2); written by bench.py --tune-dispatch",
            "device": props.name, "sms": props.multi_processor_count,
            "when": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime()), "entries": entries}
     with open(path_out, "w") as f:
@@ -897,7 +905,8 @@ def main():
             "config": {"workload": "decode_m1: one token through qkv 2560x4096, o_proj 4096x2560, "
                                    "gate_up 2560x19456, down 9728x2560; group 128; int4 weights, bf16 x/y",
                        "global_batch": 1, "parallelism": f"replicas x{world}",
-                       "l2": f"rotating {COPIES} weight copies ({COPIES * wl.bytes / 1e6:.0f} MB > 2x L2)",
+                       "l2": f"rotating {COPIES} copies of weights, scales and zero points "
+                             f"({COPIES * wl.bytes / 1e6:.0f} MB > 2x L2)",
                        "bytes_per_step": wl.bytes, "launch": "CUDA graph of the 8-copy rotation"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": traffic,
