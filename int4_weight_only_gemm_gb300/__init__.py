@@ -86,8 +86,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     return _lib
 
 
-def _stream(stream) -> int:
+# the current stream's handle without building a Stream object (a few
+# microseconds a call); the public route where this torch lacks it
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device_index: int | None = None) -> int:
     if stream is None:
+        if _raw_stream is not None:
+            return int(_raw_stream(torch.cuda.current_device() if device_index is None else device_index))
         stream = torch.cuda.current_stream()
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
@@ -286,12 +293,13 @@ def w4a16_gemm(x: torch.Tensor, qweight_dev: torch.Tensor, scales: torch.Tensor,
             workspace = _cached_workspace(need, x.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    sp = _stream(stream, x.device.index)
     if flags is None:
         st = lib.w4a16_gemm_path(path, x.data_ptr(), qweight_dev.data_ptr(), scales.data_ptr(), qzeros.data_ptr(),
-                                 M, N, K, group, out.data_ptr(), ws_ptr, ws_bytes, _stream(stream))
+                                 M, N, K, group, out.data_ptr(), ws_ptr, ws_bytes, sp)
     else:
         st = lib.w4a16_gemm_ex(path, flags, x.data_ptr(), qweight_dev.data_ptr(), scales.data_ptr(),
-                               qzeros.data_ptr(), M, N, K, group, out.data_ptr(), ws_ptr, ws_bytes, _stream(stream))
+                               qzeros.data_ptr(), M, N, K, group, out.data_ptr(), ws_ptr, ws_bytes, sp)
     _raise(st, "w4a16_gemm")
     return out
 
