@@ -13,9 +13,10 @@
 // One pipeline stage carries one group of 128 rows of K.
 //
 //  * weight producer warp: per group, into weight stage q % SW, the packed
-//    weight slab (one bulk copy, 8 KB for a full tile) and the group's
-//    zero-point words; activation producer warp: into activation stage
-//    q % SX, the x tile (one 3-D TMA, two 64-wide 128-byte swizzled slabs);
+//    weight slab (one bulk copy, 8 KB for a full tile); per chunk of 16
+//    groups, the chunk's fp16 scales and zero-point words (2-D tensor
+//    copies); activation producer warp: into activation stage q % SX, the x
+//    tile (one 3-D TMA, two 64-wide 128-byte swizzled slabs);
 //  * dequant warpgroups (four for NT <= 64, two for NT = 128 / 192), taking groups
 //    in turn: thread t copies column t's 16 words to registers (releasing
 //    the weight stage), turns them into 64 bfloat16 pairs (q - z) -- exact
@@ -31,8 +32,9 @@
 //  * rescale warpgroup(s): per group, reads D with tcgen05.ld and adds
 //    s[g][n] * D into f32 registers (the binary16 scale is applied in f32,
 //    never rounded to bfloat16); at a unit's end writes bf16 y (or, for fused
-//    gate/up weights, silu(gate) * up), or token-major split-K partials
-//    reduced in fixed order by the last CTA to arrive.
+//    gate/up weights, silu(gate) * up), or f32 split-K partials, reduced in
+//    piece order by the last CTA to arrive -- by the whole CTA once its roles
+//    are done when that piece is the CTA's last unit and NT <= 32.
 //
 // For NT >= 128 a rescale thread holds 64 or 96 accumulators: its warpgroups raise
 // their register budget (setmaxnreg) with registers the dequant warpgroups and
@@ -839,7 +841,7 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out, int force_nt) {
     const int max_split = G / 2 > 0 ? G / 2 : 1;  // at least 2 groups a piece
     long long whole = tiles;
     // Pieces of a partial last round for K of at least 16 groups, at least 5
-    // groups each.  Measured at M = 2048 with the token-major partials: the
+    // groups each.  Measured at M = 2048 with the earlier token-major partials: the
     // 4096-deep tiles of o_proj 50.1 -> 45.9 us (two pieces), the 2560-deep
     // tiles of qkv unchanged (three pieces), the 9728-deep ones of down as
     // with pieces of 8 or more.

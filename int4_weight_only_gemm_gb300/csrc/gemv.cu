@@ -18,10 +18,9 @@
 // shared-memory stages of four consecutive units (32 KB, contiguous in the
 // device layout: one bulk asynchronous copy, mbarrier transaction counts),
 // as far ahead as the ring allows, so a CTA has most of its bytes requested
-// at once and the loads never wait on the arithmetic.  The copy engine
-// spends about the same time on every copy, whatever its size, so the
-// copies are large (on this GPU a ring of 8 KB copies streams 4.5 TB/s,
-// of 16 KB or larger ones 4.9 TB/s).
+// at once and the loads never wait on the arithmetic.  One copy per stage
+// rather than per 8 KB unit: measured on gate_up at M = 1, 8.6 against
+// 10.5 us.
 // Each thread loads its column's fp16 scale and zero word itself, two units
 // ahead of use.
 //

@@ -21,7 +21,9 @@
 // copy instruction of a warp fetches contiguous runs.  Each thread streams
 // its items with 16-byte asynchronous copies into a private ring of D + 1
 // shared-memory slots, D items ahead of the one it multiplies: the distance
-// is fixed by the copies in flight, not by register scheduling.
+// is fixed by the copies in flight, not by register scheduling.  After the
+// grid-dependency wait x goes first, then the scales and the first D items;
+// the multiplication starts once x and the first item are in.
 //
 // Arithmetic: per item and token, the dot product of the 32 rows with x,
 // sum (128 + q) x, with the bfloat16 value 128 + q made by one mask-and-or
