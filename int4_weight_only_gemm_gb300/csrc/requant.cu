@@ -23,9 +23,11 @@
 // it reads the four bf16 values with one 8-byte load (a warp reads a whole
 // 256-byte tile row), and it writes the four columns' chunk words -- four
 // words each, adjacent in the device layout -- as 64 contiguous bytes.  Four
-// columns rather than eight keep the thread at 46 registers, so twice as many
-// warps are resident to cover the load latency (measured 52 us against 66 us
-// for the gate_up shape).
+// columns rather than eight keep the thread's registers down, so more warps
+// are resident to cover the load latency (measured 52 us against 66 us for
+// the gate_up shape).  The rows are read eight at a time, the next eight
+// requested while the current ones are decided (72 registers): ncu had shown
+// the warps waiting on their loads most of the time (52 -> 45 us).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -67,11 +69,23 @@ __global__ void __launch_bounds__(128) requant_pack_kernel(const uint16_t* __res
     for (int e = 0; e < C; ++e)
 #pragma unroll
         for (int j = 0; j < 4; ++j) word[e][j] = 0;
+    // the chunk's rows eight at a time, the next eight requested while the
+    // current ones are decided
+    uint2 buf[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) buf[i] = __ldcs(reinterpret_cast<const uint2*>(wp + (size_t)i * N));
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+        uint2 cur[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cur[i] = buf[i];
+        if (j < 3) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) buf[i] = __ldcs(reinterpret_cast<const uint2*>(wp + (size_t)(8 * (j + 1) + i) * N));
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {  // row 8j + i of the chunk
-            const uint2 v = *reinterpret_cast<const uint2*>(wp + (size_t)(8 * j + i) * N);
+            const uint2 v = cur[i];
             const uint32_t vw[2] = {v.x, v.y};
             const int sh = 4 * dev_nibble_pos(i);
 #pragma unroll
