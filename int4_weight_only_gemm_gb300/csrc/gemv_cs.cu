@@ -20,10 +20,12 @@
 // 128-column tile), and the lanes of a warp read adjacent columns, so each
 // copy instruction of a warp fetches contiguous runs.  Each thread streams
 // its items with 16-byte asynchronous copies into a private ring of D + 1
-// shared-memory slots, D items ahead of the one it multiplies: the distance
-// is fixed by the copies in flight, not by register scheduling.  After the
-// grid-dependency wait x goes first, then the scales and the first D items;
-// the multiplication starts once x and the first item are in.
+// shared-memory slots of IPS consecutive items (one commit group a slot), D
+// slots ahead of the one it multiplies: the distance is fixed by the copies
+// in flight, not by register scheduling, and the wait and ring bookkeeping
+// are paid once a slot.  After the grid-dependency wait x goes first, then
+// the scales and the first D slots; the multiplication starts once x and the
+// first slot are in.
 //
 // Arithmetic: per item and token, the dot product of the 32 rows with x,
 // sum (128 + q) x, with the bfloat16 value 128 + q made by one mask-and-or
@@ -62,17 +64,17 @@ constexpr int kCsThreads = 512;
 struct CsSmem {
     size_t xs, xsum, sc, zr, ring, red, total;
     static __host__ __device__ size_t up16(size_t v) { return (v + 15) & ~(size_t)15; }
-    // MT: token rows held (M rounded up), C: slice width, D: items in flight a
-    // thread.  Every region grows with C, so the widest slice of a launch sizes
-    // it for all its CTAs.
-    __host__ __device__ CsSmem(int MT, int K, int C, int D) {
+    // MT: token rows held (M rounded up), C: slice width, D: ring slots in
+    // flight a thread, IPS: items a slot.  Every region grows with C, so the
+    // widest slice of a launch sizes it for all its CTAs.
+    __host__ __device__ CsSmem(int MT, int K, int C, int D, int IPS) {
         const int G = K / 128;
         xs = 0;                                          // [MT][K] bf16 activations
         xsum = up16(xs + (size_t)MT * K * 2);            // [MT][G] f32 group sums of x
         sc = up16(xsum + (size_t)MT * G * 4);            // [G][C] fp16 scales of the slice
         zr = up16(sc + (size_t)G * C * 2);               // [G][C/4] zero words, one per run of 4 columns
-        ring = up16(zr + (size_t)G * C);                 // [D + 1][512] 16-byte item slots
-        red = ring + (size_t)(D + 1) * kCsThreads * 16;  // [S][C][MT] f32 partial sums (S C <= max(512, C))
+        ring = up16(zr + (size_t)G * C);                       // [D + 1][IPS][512] 16-byte items
+        red = ring + (size_t)(D + 1) * IPS * kCsThreads * 16;  // [S][C][MT] f32 partial sums (S C <= max(512, C))
         total = up16(red + (size_t)(C > kCsThreads ? C : kCsThreads) * MT * 4);
     }
 };
@@ -82,7 +84,7 @@ __host__ __device__ inline int cs_ranges(int C, int G) {
     return S < G ? S : G;
 }
 
-template <int MT, int D>
+template <int MT, int D, int IPS>
 __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int t = threadIdx.x;
@@ -97,12 +99,12 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
     const int C = c1 - c0;
     const int G = p.KB;
     const int S = cs_ranges(C, G);
-    const CsSmem lay(MT, p.K, C, D);
+    const CsSmem lay(MT, p.K, C, D, IPS);
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + lay.xs);
     float* xsum = reinterpret_cast<float*>(smem + lay.xsum);
     uint16_t* ssc = reinterpret_cast<uint16_t*>(smem + lay.sc);
     uint32_t* szw = reinterpret_cast<uint32_t*>(smem + lay.zr);
-    uint4* ring = reinterpret_cast<uint4*>(smem + lay.ring) + t;  // slot k of this thread at ring[k * 512]
+    uint4* ring = reinterpret_cast<uint4*>(smem + lay.ring) + t;  // item i of slot k at ring[(k IPS + i) 512]
     float* red = reinterpret_cast<float*>(smem + lay.red);
 
     // the next grid in the stream may start as soon as every CTA of this one runs
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
     const int g1 = narrow ? (int)((unsigned)(s + 1) * (unsigned)G / (unsigned)S) : (int)((long long)(s + 1) * G / S);
     const int nr = 4 * (g1 - g0);  // items of one column
     const int npass = S == 1 ? (j0 < C ? (C - j0 + kCsThreads - 1) / kCsThreads : 0) : (active ? 1 : 0);
-    const int nitems = npass * nr;
+    const int nslots = npass * nr / IPS;  // slot fills (IPS divides 4: a fill never crosses a column)
     const uint4* qd4 = reinterpret_cast<const uint4*>(p.qd);
 
     // Copy cursor over this thread's items, pass by pass: item r of column n
@@ -130,14 +132,17 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
         lstride = p.N - 128 * nb < 128 ? p.N - 128 * nb : 128;
         lptr = qd4 + (size_t)512 * p.KB * nb + (size_t)lstride * (4 * g0) + (n & 127);
     };
-    // item `issued` into its slot, one commit group per item (possibly empty)
+    // fill `issued` (IPS consecutive items of a column) into its slot, one
+    // commit group per fill (possibly empty)
     const bool passes = npass > 1;  // a thread with one column needs no column switch
     auto copy_next = [&]() {
-        if (issued < nitems) {
-            cp_async_16(ring + (size_t)lslot * kCsThreads, lptr);
+        if (issued < nslots) {
+            uint4* dst = ring + (size_t)lslot * (IPS * kCsThreads);
+#pragma unroll
+            for (int i = 0; i < IPS; ++i) cp_async_16(dst + i * kCsThreads, lptr + i * lstride);
             lslot = lslot == D ? 0 : lslot + 1;
-            lptr += lstride;
-            if (passes && ++lr == nr) {
+            lptr += IPS * lstride;
+            if (passes && (lr += IPS) == nr) {
                 lr = 0;
                 if (++lp < npass) set_column(lp);
             }
@@ -161,7 +166,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
         cp_async_commit();
     };
     auto start_items = [&]() {
-        if (nitems > 0) set_column(0);
+        if (nslots > 0) set_column(0);
 #pragma unroll 1
         for (int i = 0; i < D; ++i) copy_next();
     };
@@ -194,7 +199,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
         copy_x();
         stage_scales_zeros();
         start_items();
-        cp_async_wait<D>();  // x and the scales (the D item groups may be pending)
+        cp_async_wait<D>();  // x and the scales (the D slot groups may be pending)
     }
     __syncthreads();
     // per-group activation sums, one (token, group) per warp
@@ -215,7 +220,8 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
     const uint32_t ring_a = smem_u32(ring);
     const uint32_t xrow = (uint32_t)p.K * 2;  // bytes between token rows of xs
     constexpr int NCH = MT == 1 ? 4 : 2;  // independent chains a token
-    int kslot = 0;                        // ring slot of the item being multiplied
+    int kslot = 0;                        // ring slot of the items being multiplied
+    uint4 wk[IPS];                        // that slot's items
 #pragma unroll 1
     for (int pass = 0; pass < npass; ++pass) {
         const int jj = j0 + pass * kCsThreads;
@@ -232,10 +238,15 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
                 for (int c = 0; c < NCH; ++c) d[m][c] = 0.f;
 #pragma unroll
             for (int it = 0; it < 4; ++it) {  // the group's four items
-                cp_async_wait<D - 1>();  // this item has landed (D - 1 newer copies may be pending)
-                const uint4 w = lds_v4(ring_a + (uint32_t)kslot * (kCsThreads * 16));
-                kslot = kslot == D ? 0 : kslot + 1;
-                copy_next();  // the item D further on, into the slot the previous item used
+                if (it % IPS == 0) {
+                    cp_async_wait<D - 1>();  // this slot has landed (D - 1 newer fills may be pending)
+#pragma unroll
+                    for (int i = 0; i < IPS; ++i)
+                        wk[i] = lds_v4(ring_a + (uint32_t)(kslot * IPS + i) * (kCsThreads * 16));
+                    kslot = kslot == D ? 0 : kslot + 1;
+                    copy_next();  // the fill D further on, into the slot the previous one used
+                }
+                const uint4 w = wk[it % IPS];
                 const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
                 const int r = 4 * g + it;
 #pragma unroll
@@ -304,7 +315,15 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
 static int cs_mtile(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
 constexpr int kCsMaxSmem = 226 * 1024;
 
-// Items in flight a thread: 8, or 4 where 8 would not fit the shared memory.
+// Ring of a thread, for up to two tokens: eight items in flight, in fills of
+// two items, or of four (a whole group) where no thread holds more than two
+// groups.  Measured on the decode step (M = 1): items one at a time took
+// 4.21 / 4.63 / 8.39 / 6.87 us (qkv / o_proj / gate_up / down), fills of two
+// 3.87 / 4.37 / 8.20 / 6.67, fills of four 3.86 / 4.12 / 8.52 / 6.67 (fewer
+// instructions: 5.00 against 5.92 M on gate_up, but there the coarser waits
+// cost more than they save).  More tokens need the registers for the
+// products: single items, eight in flight, or four where eight would not fit
+// the shared memory.
 bool gemv_cs_plan(int M, int N, int K, int sms, int guH, GemvCsPlan* out) {
     if (M < 1 || M > 8 || sms < 1 || K < 128 || K % 128 || N % 8) return false;
     const int unit = guH ? 16 : 4;
@@ -314,21 +333,26 @@ bool gemv_cs_plan(int M, int N, int K, int sms, int guH, GemvCsPlan* out) {
     const int MT = cs_mtile(M);
     // the widest slice decides the shared memory
     const int C = (int)(unit * ((U + P - 1) / P));
-    int D = 8;
-    if (CsSmem(MT, K, C, D).total > (size_t)kCsMaxSmem) D = 4;
-    const CsSmem lay(MT, K, C, D);
-    if (lay.total > (size_t)kCsMaxSmem) return false;
+    const int G = K / 128, S = cs_ranges(C, G);
+    // (slots in flight, items a slot), in order of preference
+    const int forms[4][2] = {{2, 4}, {4, 2}, {8, 1}, {4, 1}};
+    int f = MT > 2 ? 2 : (G + S - 1) / S <= 2 ? 0 : 1;
+    while (f < 4 && CsSmem(MT, K, C, forms[f][0], forms[f][1]).total > (size_t)kCsMaxSmem) ++f;
+    if (f == 4) return false;
+    const int D = forms[f][0], IPS = forms[f][1];
+    const CsSmem lay(MT, K, C, D, IPS);
     out->ctas = P;
     out->U = (int)U;
     out->unit = unit;
     out->D = D;
+    out->ips = IPS;
     out->smem = lay.total;
     return true;
 }
 
-template <int MT, int D>
+template <int MT, int D, int IPS>
 static cudaError_t launch_cs(const CsParams& prm, const GemvCsPlan& plan, cudaStream_t s, bool pdl) {
-    auto kern = gemv_cs_kernel<MT, D>;
+    auto kern = gemv_cs_kernel<MT, D, IPS>;
     static int set_for[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -340,6 +364,15 @@ static cudaError_t launch_cs(const CsParams& prm, const GemvCsPlan& plan, cudaSt
         set_for[dev] = 1;
     }
     return launch_kernel(kern, dim3(plan.ctas), dim3(kCsThreads), plan.smem, s, pdl, prm);
+}
+
+template <int MT>
+static cudaError_t launch_cs_mt(const CsParams& prm, const GemvCsPlan& plan, cudaStream_t s, bool pdl) {
+    if constexpr (MT <= 2) {
+        if (plan.ips == 4) return launch_cs<MT, 2, 4>(prm, plan, s, pdl);
+        if (plan.ips == 2) return launch_cs<MT, 4, 2>(prm, plan, s, pdl);
+    }
+    return plan.D == 8 ? launch_cs<MT, 8, 1>(prm, plan, s, pdl) : launch_cs<MT, 4, 1>(prm, plan, s, pdl);
 }
 
 cudaError_t launch_gemv_cs(const uint16_t* x, const uint32_t* qd, const uint16_t* scales, const uint32_t* qzeros,
@@ -360,12 +393,11 @@ cudaError_t launch_gemv_cs(const uint16_t* x, const uint32_t* qd, const uint16_t
     const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     prm.guH = guH;
-    const bool deep = plan.D == 8;
     switch (cs_mtile(M)) {
-        case 1: return deep ? launch_cs<1, 8>(prm, plan, s, pdl) : launch_cs<1, 4>(prm, plan, s, pdl);
-        case 2: return deep ? launch_cs<2, 8>(prm, plan, s, pdl) : launch_cs<2, 4>(prm, plan, s, pdl);
-        case 4: return deep ? launch_cs<4, 8>(prm, plan, s, pdl) : launch_cs<4, 4>(prm, plan, s, pdl);
-        default: return deep ? launch_cs<8, 8>(prm, plan, s, pdl) : launch_cs<8, 4>(prm, plan, s, pdl);
+        case 1: return launch_cs_mt<1>(prm, plan, s, pdl);
+        case 2: return launch_cs_mt<2>(prm, plan, s, pdl);
+        case 4: return launch_cs_mt<4>(prm, plan, s, pdl);
+        default: return launch_cs_mt<8>(prm, plan, s, pdl);
     }
 }
 
