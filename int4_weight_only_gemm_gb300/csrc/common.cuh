@@ -246,6 +246,21 @@ W4A16_DEVICE void tma_load_3d(void* smem_dst, const void* tmap, int x, int y, in
 W4A16_DEVICE void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
+// 2-D tensor store shared -> global, in the issuing thread's bulk group
+W4A16_DEVICE void tma_store_2d(const void* tmap, const void* smem_src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
+                 "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+                 : "memory");
+}
+W4A16_DEVICE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// until at most N of this thread's bulk groups still read shared memory
+template <int N>
+W4A16_DEVICE void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// until every bulk group of this thread has completed
+W4A16_DEVICE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+W4A16_DEVICE void named_bar(int id, int count) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory"); }
 
 // ---------------------------------------------------------------------------
 // tcgen05 (tensor memory and 5th-generation MMA)
