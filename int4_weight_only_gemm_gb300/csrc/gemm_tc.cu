@@ -734,31 +734,48 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                         }
                     } else if (*sh_last) {
                         // every split's values for this thread, summed in split order,
-                        // 16 tokens at a time
+                        // TJ tokens at a time with the loads of two pieces in flight
+                        // together.  The reduction is latency-bound: 16 tokens a pass
+                        // held the reducing CTA ~9.6 us on a three-piece 192-token
+                        // tile; 32 a pass (where the register split leaves room) took
+                        // the prefill step 348 -> 345 us, three pieces a round spilled
+                        // and was slower (359 us).
+                        constexpr int TJ = C::kRegSplit ? 32 : 16;
+                        constexpr int PK = 2;
                         const float4* base = reinterpret_cast<const float4*>(p.partials) +
                                              ((size_t)tile * ui.ns * (NT / 4) + r * (CW / 4)) * 128 + t;
                         const size_t sstride = (size_t)(NT / 4) * 128;  // float4s between splits
 #pragma unroll 1
-                        for (int j0 = 0; j0 < CW; j0 += 16) {
-                            float4 sum[4];
+                        for (int j0 = 0; j0 < CW; j0 += TJ) {
+                            float4 sum[TJ / 4];
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-                            for (int sp = 0; sp < ui.ns; ++sp) {
+                            for (int i = 0; i < TJ / 4; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+                            for (int sp0 = 0; sp0 < ui.ns; sp0 += PK) {
+                                float4 v[PK][TJ / 4];
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const float4 v = __ldcg(base + sp * sstride + (size_t)(j0 / 4 + i) * 128);
-                                    sum[i].x += v.x;
-                                    sum[i].y += v.y;
-                                    sum[i].z += v.z;
-                                    sum[i].w += v.w;
-                                }
+                                for (int k = 0; k < PK; ++k)
+#pragma unroll
+                                    for (int i = 0; i < TJ / 4; ++i)
+                                        v[k][i] = sp0 + k < ui.ns
+                                                      ? __ldcg(base + (sp0 + k) * sstride + (size_t)(j0 / 4 + i) * 128)
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                                for (int k = 0; k < PK; ++k)
+                                    if (sp0 + k < ui.ns)
+#pragma unroll
+                                        for (int i = 0; i < TJ / 4; ++i) {
+                                            sum[i].x += v[k][i].x;
+                                            sum[i].y += v[k][i].y;
+                                            sum[i].z += v[k][i].z;
+                                            sum[i].w += v[k][i].w;
+                                        }
                             }
                             if (p.guH) {
                                 const bool gate = !(t & 8);
                                 const size_t col = (size_t)gu_column(gate ? n : n - 8, p.guH);
 #pragma unroll
-                                for (int j = 0; j < 16; j += 2) {
+                                for (int j = 0; j < TJ; j += 2) {
                                     const float4& v = sum[j / 4];
                                     const float a0 = (j & 2) ? v.z : v.x, a1 = (j & 2) ? v.w : v.y;
                                     const float r = __shfl_xor_sync(0xFFFFFFFFu, gate ? a1 : a0, 8);
@@ -769,7 +786,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                                 }
                             } else if (t < W) {
 #pragma unroll
-                                for (int j = 0; j < 16; ++j) {
+                                for (int j = 0; j < TJ; ++j) {
                                     const float4& v = sum[j / 4];
                                     const float val = (j & 3) == 0 ? v.x : (j & 3) == 1 ? v.y : (j & 3) == 2 ? v.z : v.w;
                                     if (j0 + j < CW && tok0 + j0 + j < p.M)
