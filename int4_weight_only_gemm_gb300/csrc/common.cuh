@@ -175,6 +175,9 @@ W4A16_DEVICE bool bar_and(int id, int count, bool pred) {
 }
 
 // explicit shared-memory loads (32-bit shared addresses)
+W4A16_DEVICE void sts_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
 W4A16_DEVICE uint4 lds_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -246,20 +249,6 @@ W4A16_DEVICE void tma_load_3d(void* smem_dst, const void* tmap, int x, int y, in
 W4A16_DEVICE void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
-// 2-D tensor store shared -> global, in the issuing thread's bulk group
-W4A16_DEVICE void tma_store_2d(const void* tmap, const void* smem_src, int x, int y) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
-                 "r"(smem_u32(smem_src)), "r"(x), "r"(y)
-                 : "memory");
-}
-W4A16_DEVICE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// until at most N of this thread's bulk groups still read shared memory
-template <int N>
-W4A16_DEVICE void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// until every bulk group of this thread has completed
-W4A16_DEVICE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 W4A16_DEVICE void named_bar(int id, int count) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory"); }
 
 // ---------------------------------------------------------------------------

@@ -32,8 +32,8 @@
 //  * rescale warpgroup(s): per group, reads D with tcgen05.ld and adds
 //    s[g][n] * D into f32 registers (the binary16 scale is applied in f32,
 //    never rounded to bfloat16); at a unit's end writes bf16 y (with 192-token
-//    tiles through shared memory, 16 tokens x 128 columns per tensor store;
-//    for fused gate/up weights silu(gate) * up), or f32 split-K partials, reduced in
+//    tiles through shared memory, 16 tokens at a time, as 16-byte rows; for
+//    fused gate/up weights silu(gate) * up), or f32 split-K partials, reduced in
 //    piece order by the last CTA to arrive -- by the whole CTA once its roles
 //    are done when that piece is the CTA's last unit and NT <= 32.
 //
@@ -81,7 +81,7 @@ struct TcParams {
     int prefetch;    // weights may be loaded before the preceding grid completes
     int guH;         // > 0: fused gate/up weights (N = 2 guH); y[M][guH] = silu(gate) * up
     int zmap;        // tmap_z describes the zero words (N % 32 == 0); otherwise the lanes copy them
-    int ymap;        // tmap_y describes y: whole tiles leave through shared memory and tensor stores
+    int ymap;        // y is 16-byte aligned: whole tiles leave through shared memory in 16-byte rows
 };
 
 // Groups of K per activation stage (the box of the activations' tensor map
@@ -154,11 +154,13 @@ struct TcCfg {
     static constexpr int kMetaBytes = kMetaScl + 2 * GB * 8 * 4;
     static constexpr int kMetaOff = kPOff + SW * WP * 8192;
     static constexpr int kBarOff = kMetaOff + MB * kMetaBytes;
-    // y staging (NT = 192): per rescale warpgroup kYB buffers of 16 tokens x
-    // 128 columns of bf16, the box of one tensor store.  Measured against
-    // direct 2-byte stores: gate_up at M = 2048 174.8 -> 169.7 us, M = 8192
-    // 658 -> 640 us (one weight stage fewer to make room); with 64- and
-    // 128-token tiles (M = 64, 128) slightly slower, so not used there.
+    // y staging (NT = 192): per rescale warpgroup two buffers of 16 tokens x
+    // 128 columns of bf16, stored as 16-byte rows.  Measured against direct
+    // 2-byte stores from the rescale threads: gate_up at M = 2048 174.8 ->
+    // 167.0 us (one weight stage fewer to make room); with 16-token tensor
+    // stores from the buffers 169.7 us (their reads of shared memory wait
+    // behind the activation loads); with 64- and 128-token tiles staging was
+    // slightly slower (M = 64, 128), so not used there.
     static constexpr bool kYStore = NT >= 192;
     static constexpr int kYB = 2, kYBytes = 16 * 128 * 2;
     static constexpr int kYOff = kBarOff + 1024;
@@ -219,8 +221,7 @@ W4A16_DEVICE void tmem_st_x32(uint32_t taddr, const uint32_t* v) {
 template <int NT>
 __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_s,
-                   const __grid_constant__ CUtensorMap tmap_z, const __grid_constant__ CUtensorMap tmap_y,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmap_z, const TcParams p) {
     using C = TcCfg<NT>;
     constexpr int SX = C::SX;
     constexpr int SW = C::SW;
@@ -279,7 +280,6 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
             prefetch_tmap(&tmap_x);
             prefetch_tmap(&tmap_s);
             if (p.zmap) prefetch_tmap(&tmap_z);
-            if (p.ymap) prefetch_tmap(&tmap_y);
         }
     }
     tc_fence_before();
@@ -661,28 +661,31 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                         }
                     } else if (C::kYStore && p.ymap) {
                         // Per 16 tokens: every thread writes its column into a
-                        // staging buffer, one thread stores the [16][128] box
-                        // (columns past N and tokens past M are not written); a
-                        // buffer is rewritten once its previous store has read it.
+                        // staging buffer; after the warpgroup's barrier each thread
+                        // stores 16 contiguous bytes (8 columns) of two token rows.
+                        // Chunk k uses buffer k % 2: its writes follow the barrier of
+                        // chunk k - 1, after which nobody reads chunk k - 2's buffer.
                         unsigned char* ybase = smem + C::kYOff + r * (C::kYB * C::kYBytes);
+                        const int cx = 8 * (t & 15);  // this thread's columns in the box
 #pragma unroll
                         for (int c = 0; c < CW / 16; ++c) {
                             if (tok0 + 16 * c >= p.M) break;  // uniform in the warpgroup
-                            if (ych >= C::kYB) {
-                                if (t == 0) bulk_wait_read<C::kYB - 1>();
-                                named_bar(6 + r, 128);
-                            }
-                            uint16_t* buf = reinterpret_cast<uint16_t*>(ybase + (ych % C::kYB) * C::kYBytes);
+                            const uint32_t buf = smem_u32(ybase + (ych & 1) * C::kYBytes);
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 const int j = 16 * c + i;
-                                buf[i * 128 + t] = f32_to_bf16_rn((j & 1) ? acc[j / 2].y : acc[j / 2].x);
+                                sts_u16(buf + (uint32_t)(i * 256 + 2 * t),
+                                        f32_to_bf16_rn((j & 1) ? acc[j / 2].y : acc[j / 2].x));
                             }
-                            fence_proxy_async_smem();
                             named_bar(6 + r, 128);
-                            if (t == 0) {
-                                tma_store_2d(&tmap_y, buf, 128 * ui.nb, tok0 + 16 * c);
-                                bulk_commit();
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int row = (t >> 4) + 8 * h;
+                                const int tok = tok0 + 16 * c + row;
+                                const int col = 128 * ui.nb + cx;
+                                const uint4 v = lds_v4(buf + (uint32_t)(row * 256 + 2 * cx));
+                                if (tok < p.M && col < p.N)  // N % 8 == 0: all 8 columns or none
+                                    *reinterpret_cast<uint4*>(p.y + (size_t)tok * p.N + col) = v;
                             }
                             ++ych;
                         }
@@ -802,8 +805,6 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < CW / 2; ++j) acc[j] = make_float2(0.f, 0.f);
         }
-        // the staged stores complete before the CTA may exit
-        if (C::kYStore && t == 0 && ych > 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -965,8 +966,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 template <int NT>
-static cudaError_t launch_nt(const CUtensorMap& tm, const CUtensorMap& tms, const CUtensorMap& tmz,
-                             const CUtensorMap& tmy, const TcParams& prm, const TcPlan& plan, cudaStream_t s, bool pdl) {
+static cudaError_t launch_nt(const CUtensorMap& tm, const CUtensorMap& tms, const CUtensorMap& tmz, const TcParams& prm,
+                             const TcPlan& plan, cudaStream_t s, bool pdl) {
     using C = TcCfg<NT>;
     auto kern = tc_gemm_kernel<NT>;
     static int set_for[64];  // shared memory limit raised once per device
@@ -987,7 +988,7 @@ static cudaError_t launch_nt(const CUtensorMap& tm, const CUtensorMap& tms, cons
         }
         set_for[dev] = 1;
     }
-    return launch_kernel(kern, dim3(plan.ctas), dim3(C::kThreads), plan.smem, s, pdl, tm, tms, tmz, tmy, prm);
+    return launch_kernel(kern, dim3(plan.ctas), dim3(C::kThreads), plan.smem, s, pdl, tm, tms, tmz, prm);
 }
 
 
@@ -1035,20 +1036,8 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
-    // y [M][N] bf16 for the staged epilogue of whole tiles (NT = 192, plain
-    // weights): boxes of 16 tokens x 128 columns; the base must be 16-byte
-    // aligned (rows are, N % 8 == 0)
-    const int ymap = plan.NT >= 192 && !guH && M >= 16 && N >= 128 && ((uintptr_t)y & 15) == 0;
-    CUtensorMap tmy = tms;
-    if (ymap) {
-        const cuuint64_t yd[2] = {(cuuint64_t)N, (cuuint64_t)M};
-        const cuuint64_t ys[1] = {(cuuint64_t)N * 2};
-        const cuuint32_t yb[2] = {128, 16};
-        const cuuint32_t ye[2] = {1, 1};
-        r = encode(&tmy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, yd, ys, yb, ye, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    }
+    // staged epilogue of whole tiles (NT = 192, plain weights): 16-byte rows of y
+    const int ymap = plan.NT >= 192 && !guH && ((uintptr_t)y & 15) == 0;
     TcParams prm;
     prm.qd = qd;
     prm.scales = scales;
@@ -1072,11 +1061,11 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
     prm.zmap = zmap;
     prm.ymap = ymap;
     switch (plan.NT) {
-        case 16: return launch_nt<16>(tm, tms, tmz, tmy, prm, plan, s, pdl);
-        case 32: return launch_nt<32>(tm, tms, tmz, tmy, prm, plan, s, pdl);
-        case 64: return launch_nt<64>(tm, tms, tmz, tmy, prm, plan, s, pdl);
-        case 192: return launch_nt<192>(tm, tms, tmz, tmy, prm, plan, s, pdl);
-        default: return launch_nt<128>(tm, tms, tmz, tmy, prm, plan, s, pdl);
+        case 16: return launch_nt<16>(tm, tms, tmz, prm, plan, s, pdl);
+        case 32: return launch_nt<32>(tm, tms, tmz, prm, plan, s, pdl);
+        case 64: return launch_nt<64>(tm, tms, tmz, prm, plan, s, pdl);
+        case 192: return launch_nt<192>(tm, tms, tmz, prm, plan, s, pdl);
+        default: return launch_nt<128>(tm, tms, tmz, prm, plan, s, pdl);
     }
 }
 
