@@ -78,6 +78,10 @@ struct TcParams {
     int whole;       // units [0, whole) are whole tiles: unit u is tile u
     int splits;      // units from `whole` on: each later tile in `splits` K pieces
     int units;       // whole + (tiles - whole) * splits
+    // n / splits and n / NB by multiply and shift (FastDiv below; every role
+    // decodes each unit, and four dependent divisions took ~0.4 us)
+    uint32_t msplits, mnb;
+    int ssplits, snb;
     int prefetch;    // weights may be loaded before the preceding grid completes
     int guH;         // > 0: fused gate/up weights (N = 2 guH); y[M][guH] = silu(gate) * up
     int zmap;        // tmap_z describes the zero words (N % 32 == 0); otherwise the lanes copy them
@@ -175,6 +179,26 @@ struct TcCfg {
     static_assert(kTmemUsed <= 512, "tensor memory budget");
 };
 
+// Division by a divisor d >= 1 fixed for the launch, for numerators
+// 0 <= n < 2^31, by one multiply-high and a shift (Granlund and Montgomery,
+// "Division by invariant integers using multiplication", 1994, theorem 4.2
+// with N = 31): with l = ceil(log2 d) and m = ceil(2^(31 + l) / d), which is
+// below 2^32, floor(n / d) = floor(m n / 2^(31 + l)).  m = 0 stands for d = 1.
+struct FastDiv {
+    uint32_t m;
+    int s;  // l - 1
+};
+static inline FastDiv fast_div(int d) {
+    FastDiv f{0u, 0};
+    if (d <= 1) return f;
+    int l = 0;
+    while ((1ll << l) < d) ++l;
+    f.m = (uint32_t)(((1ull << (31 + l)) + (unsigned long long)d - 1) / (unsigned long long)d);
+    f.s = l - 1;
+    return f;
+}
+W4A16_DEVICE int div_by(int n, uint32_t m, int s) { return m ? (int)(__umulhi((uint32_t)n, m) >> s) : n; }
+
 struct UnitInfo {
     int nb, mb, split, ns, g0, g1;
     int ptile;  // for a K piece (ns > 1): index of its tile among the split tiles
@@ -194,16 +218,16 @@ __device__ __forceinline__ UnitInfo unit_info(const TcParams& p, int u) {
         r.ns = 1;
         r.ptile = -1;
     } else {
-        r.ptile = u / p.splits;
+        r.ptile = div_by(u, p.msplits, p.ssplits);
         r.split = u - r.ptile * p.splits;
         r.ns = p.splits;
         tile = p.whole + r.ptile;
     }
-    r.nb = tile % p.NB;
-    r.mb = tile / p.NB;
-    // unsigned 32-bit: split < ns <= CTAs (< 256) and G < 2^24, so no overflow
-    r.g0 = (int)((unsigned)r.split * (unsigned)p.G / (unsigned)r.ns);
-    r.g1 = (int)((unsigned)(r.split + 1) * (unsigned)p.G / (unsigned)r.ns);
+    r.mb = div_by(tile, p.mnb, p.snb);
+    r.nb = tile - r.mb * p.NB;
+    // (split + 1) G < 2^31 (checked by the planner)
+    r.g0 = r.ns == 1 ? 0 : div_by(r.split * p.G, p.msplits, p.ssplits);
+    r.g1 = r.ns == 1 ? p.G : div_by((r.split + 1) * p.G, p.msplits, p.ssplits);
     return r;
 }
 
@@ -930,7 +954,7 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out, int force_nt) {
         splits = 1;
     }
     const long long units = whole + (tiles - whole) * splits;
-    if (units >= (1ll << 31)) return false;
+    if (units >= (1ll << 31) || tiles >= (1ll << 31) || (long long)splits * G >= (1ll << 31)) return false;
     out->NT = NT;
     out->MT = MT;
     out->NB = L.NB;
@@ -1055,6 +1079,11 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
     prm.whole = plan.whole;
     prm.splits = plan.splits;
     prm.units = plan.units;
+    const FastDiv fs = fast_div(plan.splits), fn = fast_div(plan.NB);
+    prm.msplits = fs.m;
+    prm.ssplits = fs.s;
+    prm.mnb = fn.m;
+    prm.snb = fn.s;
     const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     prm.guH = guH;
