@@ -179,26 +179,6 @@ struct TcCfg {
     static_assert(kTmemUsed <= 512, "tensor memory budget");
 };
 
-// Division by a divisor d >= 1 fixed for the launch, for numerators
-// 0 <= n < 2^31, by one multiply-high and a shift (Granlund and Montgomery,
-// "Division by invariant integers using multiplication", 1994, theorem 4.2
-// with N = 31): with l = ceil(log2 d) and m = ceil(2^(31 + l) / d), which is
-// below 2^32, floor(n / d) = floor(m n / 2^(31 + l)).  m = 0 stands for d = 1.
-struct FastDiv {
-    uint32_t m;
-    int s;  // l - 1
-};
-static inline FastDiv fast_div(int d) {
-    FastDiv f{0u, 0};
-    if (d <= 1) return f;
-    int l = 0;
-    while ((1ll << l) < d) ++l;
-    f.m = (uint32_t)(((1ull << (31 + l)) + (unsigned long long)d - 1) / (unsigned long long)d);
-    f.s = l - 1;
-    return f;
-}
-W4A16_DEVICE int div_by(int n, uint32_t m, int s) { return m ? (int)(__umulhi((uint32_t)n, m) >> s) : n; }
-
 struct UnitInfo {
     int nb, mb, split, ns, g0, g1;
     int ptile;  // for a K piece (ns > 1): index of its tile among the split tiles

@@ -55,6 +55,16 @@ struct CsParams {
     int U, unit;      // column units and their width (4, or 16 for fused gate/up)
     int prefetch;     // weights, scales and zeros may be read before the preceding grid completes
     int guH;          // > 0: fused gate/up weights (N = 2 guH); y[M][guH] = silu(gate) * up
+    // CTA b owns column units [b U / P, (b + 1) U / P): slices of Cw[0] or
+    // Cw[1] columns, with Sr[k] K ranges; the divisions by P, by the slice
+    // width, by the range count and by a quarter of the width are multiplies
+    // and shifts (FastDiv: four dependent divisions sat between a CTA's start
+    // and its first weight copy)
+    uint32_t mP;
+    int sP;
+    int Cw[2], Sr[2];
+    uint32_t mC[2], mS[2], mC4[2];
+    int sC[2], sS[2], sC4[2];
 };
 
 constexpr int kCsThreads = 512;
@@ -89,16 +99,13 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
     extern __shared__ __align__(128) unsigned char smem[];
     const int t = threadIdx.x;
     const int b = blockIdx.x;
-    const int P = (int)gridDim.x;
-    // slice bounds: 32-bit arithmetic where the products fit (a 64-bit
-    // division costs tens of instructions, paid by every thread)
-    const bool narrow = p.U < (1 << 22) && p.KB < (1 << 22);
-    const int c0 = p.unit * (narrow ? (int)((unsigned)b * (unsigned)p.U / (unsigned)P) : (int)((long long)b * p.U / P));
-    const int c1 = p.unit * (narrow ? (int)((unsigned)(b + 1) * (unsigned)p.U / (unsigned)P)
-                                    : (int)((long long)(b + 1) * p.U / P));
+    // slice bounds ((b + 1) U < 2^31 and S G < 2^31: checked by the planner)
+    const int c0 = p.unit * div_by(b * p.U, p.mP, p.sP);
+    const int c1 = p.unit * div_by((b + 1) * p.U, p.mP, p.sP);
     const int C = c1 - c0;
+    const int kw = C == p.Cw[0] ? 0 : 1;  // which of the two slice widths
     const int G = p.KB;
-    const int S = cs_ranges(C, G);
+    const int S = p.Sr[kw];
     const CsSmem lay(MT, p.K, C, D, IPS);
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + lay.xs);
     float* xsum = reinterpret_cast<float*>(smem + lay.xsum);
@@ -112,10 +119,10 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
 
     // this thread's work: column j0 (then j0 + 512, ... when S == 1), groups [g0, g1)
     const bool active = t < S * C || S == 1;
-    const int j0 = S == 1 ? t : t % C;
-    const int s = S == 1 ? 0 : t / C;
-    const int g0 = narrow ? (int)((unsigned)s * (unsigned)G / (unsigned)S) : (int)((long long)s * G / S);
-    const int g1 = narrow ? (int)((unsigned)(s + 1) * (unsigned)G / (unsigned)S) : (int)((long long)(s + 1) * G / S);
+    const int s = S == 1 ? 0 : div_by(t, p.mC[kw], p.sC[kw]);
+    const int j0 = S == 1 ? t : t - s * C;
+    const int g0 = div_by(s * G, p.mS[kw], p.sS[kw]);
+    const int g1 = div_by((s + 1) * G, p.mS[kw], p.sS[kw]);
     const int nr = 4 * (g1 - g0);  // items of one column
     const int npass = S == 1 ? (j0 < C ? (C - j0 + kCsThreads - 1) / kCsThreads : 0) : (active ? 1 : 0);
     const int nslots = npass * nr / IPS;  // slot fills (IPS divides 4: a fill never crosses a column)
@@ -157,7 +164,7 @@ __global__ void __launch_bounds__(kCsThreads, 1) gemv_cs_kernel(const CsParams p
     auto stage_scales_zeros = [&]() {
         const int C4 = C >> 2;
         for (int i = t; i < G * C4; i += kCsThreads) {
-            const int g = i / C4, jj = 4 * (i - g * C4);
+            const int g = div_by(i, p.mC4[kw], p.sC4[kw]), jj = 4 * (i - g * C4);
             const int n = c0 + jj;
             const int cn = p.guH ? gu_column(n, p.guH) : n;
             cp_async_8(ssc + (size_t)g * C + jj, p.scales + (size_t)g * p.N + cn);
@@ -330,6 +337,8 @@ bool gemv_cs_plan(int M, int N, int K, int sms, int guH, GemvCsPlan* out) {
     if (N % unit) return false;
     const long long U = N / unit;
     const int P = (int)(U < sms ? U : sms);
+    // the kernel's slice arithmetic stays below 2^31: (b + 1) U and S G (S <= 512)
+    if ((long long)(P + 1) * U >= (1ll << 31) || (long long)(K / 128) * kCsThreads >= (1ll << 31)) return false;
     const int MT = cs_mtile(M);
     // the widest slice decides the shared memory
     const int C = (int)(unit * ((U + P - 1) / P));
@@ -390,6 +399,22 @@ cudaError_t launch_gemv_cs(const uint16_t* x, const uint32_t* qd, const uint16_t
     prm.KB = K / 128;
     prm.U = plan.U;
     prm.unit = plan.unit;
+    const FastDiv fp = fast_div(plan.ctas);
+    prm.mP = fp.m;
+    prm.sP = fp.s;
+    for (int k = 0; k < 2; ++k) {
+        const int cw = plan.unit * (plan.U / plan.ctas + k);
+        const int sr = cs_ranges(cw, K / 128);
+        const FastDiv fc = fast_div(cw), fs = fast_div(sr), fc4 = fast_div(cw / 4);
+        prm.Cw[k] = cw;
+        prm.Sr[k] = sr;
+        prm.mC[k] = fc.m;
+        prm.sC[k] = fc.s;
+        prm.mS[k] = fs.m;
+        prm.sS[k] = fs.s;
+        prm.mC4[k] = fc4.m;
+        prm.sC4[k] = fc4.s;
+    }
     const bool pdl = (flags & W4A16_FLAG_PDL) != 0;
     prm.prefetch = pdl && (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     prm.guH = guH;
