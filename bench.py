@@ -836,8 +836,13 @@ def main():
         small = unit == "GB/s"
         copies = COPIES if small else 2
         wl2 = Workload(w, torch, items, seed, copies, device)
-        ps, rt = wl2.graphs()
         n = 4000 if small else 40
+        # the step as the headline's: PDL chain with static weights; the plain
+        # PDL chain beside it
+        ps, rt = wl2.graphs()
+        t_pdl = time_graph_steps(torch, ps, rt, copies, n, 10)
+        del ps, rt
+        ps, rt = wl2.graphs(flags=HEADLINE_FLAGS)
         t_ms = time_graph_steps(torch, ps, rt, copies, n, 10)
         if unit == "GB/s":
             v = wl2.bytes * n / (t_ms / 1e3) / 1e9
@@ -855,6 +860,7 @@ def main():
                                 "TFLOP/s": gemm_flops(g["M"], g["K"], g["N"]) * n1 / (t1 / 1e3) / 1e12}
             del ps1, rt1
         extra[name] = {"value": v, "unit": unit, "frac": frac, "ms_per_step": t_ms / n,
+                       "launch": "PDL chain, static weights (flags 3)", "ms_per_step_pdl_only": t_pdl / n,
                        "workload": ", ".join(f"{s} M={M}" for s, M in items), "per_gemm": per2}
         del ps, rt, wl2
         torch.cuda.empty_cache()
@@ -866,7 +872,7 @@ def main():
         for b in (1, 2, 3, 4):
             M = 16 * b
             wl3 = Workload(w, torch, [(s, M) for s in wi.LAYER], 2, COPIES, device)
-            ps, rt = wl3.graphs()
+            ps, rt = wl3.graphs(flags=HEADLINE_FLAGS)
             n = 2000
             t_ms = time_graph_steps(torch, ps, rt, COPIES, n, 10)
             us = t_ms / n * 1e3
