@@ -354,7 +354,8 @@ def measure_e2e(w, torch, wl, steps):
         c = i % wl.copies
         dx.copy_(hx, non_blocking=True)
         for j, g in enumerate(wl.gemms):
-            w.w4a16_gemm(dxs[j], g["qds"][c], g["scs"][c], g["qzs"][c], out=dys[j], workspace=g["ws"])
+            w.w4a16_gemm(dxs[j], g["qds"][c], g["scs"][c], g["qzs"][c], out=dys[j], workspace=g["ws"],
+                         flags=HEADLINE_FLAGS)
         hy.copy_(dy, non_blocking=True)
         stream.synchronize()
 

@@ -49,6 +49,8 @@ class W4A16Error(RuntimeError):
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     """Loads the compiled library; raises if it has not been built."""
     global _lib
+    if _lib is not None:  # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(path):
