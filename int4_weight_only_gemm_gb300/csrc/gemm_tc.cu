@@ -85,7 +85,7 @@ struct TcParams {
     int prefetch;    // weights may be loaded before the preceding grid completes
     int guH;         // > 0: fused gate/up weights (N = 2 guH); y[M][guH] = silu(gate) * up
     int zmap;        // tmap_z describes the zero words (N % 32 == 0); otherwise the lanes copy them
-    int ymap;        // y is 16-byte aligned: whole tiles leave through shared memory in 16-byte rows
+    int ymap;        // y is 16-byte aligned: whole tiles leave through shared memory in 16-byte rows (NT = 192)
 };
 
 // Groups of K per activation stage (the box of the activations' tensor map
@@ -649,7 +649,58 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
             const int tok0 = ui.mb * NT + r * CW;
             if (all_ok) {
                 if (ui.ns == 1) {
-                    if (p.guH) {
+                    if (C::kYStore && p.ymap) {
+                        // Per 16 tokens: every thread writes its values into a
+                        // staging buffer; after the warpgroup's barrier each thread
+                        // stores 16 contiguous bytes of a token row.  Chunk k uses
+                        // buffer k % 2: its writes follow the barrier of chunk k - 1,
+                        // after which nobody reads chunk k - 2's buffer.  Fused
+                        // gate/up weights: a row holds the tile's 64 outputs, thread
+                        // t (gate lane, t % 16 < 8) the even tokens of output
+                        // 8 (t / 16) + t % 8 and its up lane t + 8 the odd ones.
+                        unsigned char* ybase = smem + C::kYOff + r * (C::kYB * C::kYBytes);
+#pragma unroll
+                        for (int c = 0; c < CW / 16; ++c) {
+                            if (tok0 + 16 * c >= p.M) break;  // uniform in the warpgroup
+                            const uint32_t buf = smem_u32(ybase + (ych & 1) * C::kYBytes);
+                            if (p.guH) {
+                                const bool gate = !(t & 8);
+                                const int oc = 8 * (t >> 4) + (t & 7);
+#pragma unroll
+                                for (int i = 0; i < 16; i += 2) {
+                                    const float a0 = acc[(16 * c + i) / 2].x, a1 = acc[(16 * c + i) / 2].y;
+                                    const float o = __shfl_xor_sync(0xFFFFFFFFu, gate ? a1 : a0, 8);
+                                    const int row = i + (gate ? 0 : 1);
+                                    sts_u16(buf + (uint32_t)(row * 128 + 2 * oc),
+                                            f32_to_bf16_rn(gate ? silu_mul(a0, o) : silu_mul(o, a1)));
+                                }
+                                named_bar(6 + r, 128);
+                                const int row = t >> 3, tok = tok0 + 16 * c + row;
+                                const uint4 v = lds_v4(buf + (uint32_t)(row * 128 + 16 * (t & 7)));
+                                if (tok < p.M)
+                                    *reinterpret_cast<uint4*>(p.y + (size_t)tok * p.guH + 64 * ui.nb + 8 * (t & 7)) = v;
+                            } else {
+                                const int cx = 8 * (t & 15);  // this thread's columns in the row
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    const int j = 16 * c + i;
+                                    sts_u16(buf + (uint32_t)(i * 256 + 2 * t),
+                                            f32_to_bf16_rn((j & 1) ? acc[j / 2].y : acc[j / 2].x));
+                                }
+                                named_bar(6 + r, 128);
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    const int row = (t >> 4) + 8 * h;
+                                    const int tok = tok0 + 16 * c + row;
+                                    const int col = 128 * ui.nb + cx;
+                                    const uint4 v = lds_v4(buf + (uint32_t)(row * 256 + 2 * cx));
+                                    if (tok < p.M && col < p.N)  // N % 8 == 0: all 8 columns or none
+                                        *reinterpret_cast<uint4*>(p.y + (size_t)tok * p.N + col) = v;
+                                }
+                            }
+                            ++ych;
+                        }
+                    } else if (p.guH) {
                         // Thread t (t % 16 < 8) holds a gate column, thread t + 8 its
                         // up column.  Per pair of tokens one value crosses each way: the
                         // gate lane finishes token j, the up lane token j + 1.
@@ -662,36 +713,6 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
                             const int tok = tok0 + j + (gate ? 0 : 1);
                             if (tok < p.M)
                                 p.y[(size_t)tok * p.guH + col] = f32_to_bf16_rn(gate ? silu_mul(a0, r) : silu_mul(r, a1));
-                        }
-                    } else if (C::kYStore && p.ymap) {
-                        // Per 16 tokens: every thread writes its column into a
-                        // staging buffer; after the warpgroup's barrier each thread
-                        // stores 16 contiguous bytes (8 columns) of two token rows.
-                        // Chunk k uses buffer k % 2: its writes follow the barrier of
-                        // chunk k - 1, after which nobody reads chunk k - 2's buffer.
-                        unsigned char* ybase = smem + C::kYOff + r * (C::kYB * C::kYBytes);
-                        const int cx = 8 * (t & 15);  // this thread's columns in the box
-#pragma unroll
-                        for (int c = 0; c < CW / 16; ++c) {
-                            if (tok0 + 16 * c >= p.M) break;  // uniform in the warpgroup
-                            const uint32_t buf = smem_u32(ybase + (ych & 1) * C::kYBytes);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int j = 16 * c + i;
-                                sts_u16(buf + (uint32_t)(i * 256 + 2 * t),
-                                        f32_to_bf16_rn((j & 1) ? acc[j / 2].y : acc[j / 2].x));
-                            }
-                            named_bar(6 + r, 128);
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const int row = (t >> 4) + 8 * h;
-                                const int tok = tok0 + 16 * c + row;
-                                const int col = 128 * ui.nb + cx;
-                                const uint4 v = lds_v4(buf + (uint32_t)(row * 256 + 2 * cx));
-                                if (tok < p.M && col < p.N)  // N % 8 == 0: all 8 columns or none
-                                    *reinterpret_cast<uint4*>(p.y + (size_t)tok * p.N + col) = v;
-                            }
-                            ++ych;
                         }
                     } else if (t < W) {
 #pragma unroll
@@ -1040,8 +1061,8 @@ cudaError_t launch_tc(const uint16_t* x, const uint32_t* qd, const uint16_t* sca
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
-    // staged epilogue of whole tiles (NT = 192, plain weights): 16-byte rows of y
-    const int ymap = plan.NT >= 192 && !guH && ((uintptr_t)y & 15) == 0;
+    // staged epilogue of whole tiles (NT = 192): 16-byte rows of y
+    const int ymap = plan.NT >= 192 && ((uintptr_t)y & 15) == 0;
     TcParams prm;
     prm.qd = qd;
     prm.scales = scales;
