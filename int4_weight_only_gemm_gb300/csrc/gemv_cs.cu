@@ -323,14 +323,15 @@ static int cs_mtile(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
 constexpr int kCsMaxSmem = 226 * 1024;
 
 // Ring of a thread, for up to two tokens: eight items in flight, in fills of
-// two items, or of four (a whole group) where no thread holds more than two
-// groups.  Measured on the decode step (M = 1): items one at a time took
+// two items.  Measured on the decode step (M = 1): items one at a time took
 // 4.21 / 4.63 / 8.39 / 6.87 us (qkv / o_proj / gate_up / down), fills of two
 // 3.87 / 4.37 / 8.20 / 6.67, fills of four 3.86 / 4.12 / 8.52 / 6.67 (fewer
 // instructions: 5.00 against 5.92 M on gate_up, but there the coarser waits
-// cost more than they save).  More tokens need the registers for the
-// products: single items, eight in flight, or four where eight would not fit
-// the shared memory.
+// cost more than they save); with the prologue's divisions replaced, fills
+// of two everywhere (3.61 / 4.11 / 7.90 / 6.41, step 21.1 us) beat fills of
+// four for qkv and o_proj (3.86 / 4.11, step 21.2 us).  More tokens need the
+// registers for the products: single items, eight in flight, or four where
+// eight would not fit the shared memory.
 bool gemv_cs_plan(int M, int N, int K, int sms, int guH, GemvCsPlan* out) {
     if (M < 1 || M > 8 || sms < 1 || K < 128 || K % 128 || N % 8) return false;
     const int unit = guH ? 16 : 4;
@@ -342,12 +343,11 @@ bool gemv_cs_plan(int M, int N, int K, int sms, int guH, GemvCsPlan* out) {
     const int MT = cs_mtile(M);
     // the widest slice decides the shared memory
     const int C = (int)(unit * ((U + P - 1) / P));
-    const int G = K / 128, S = cs_ranges(C, G);
     // (slots in flight, items a slot), in order of preference
-    const int forms[4][2] = {{2, 4}, {4, 2}, {8, 1}, {4, 1}};
-    int f = MT > 2 ? 2 : (G + S - 1) / S <= 2 ? 0 : 1;
-    while (f < 4 && CsSmem(MT, K, C, forms[f][0], forms[f][1]).total > (size_t)kCsMaxSmem) ++f;
-    if (f == 4) return false;
+    const int forms[3][2] = {{4, 2}, {8, 1}, {4, 1}};
+    int f = MT > 2 ? 1 : 0;
+    while (f < 3 && CsSmem(MT, K, C, forms[f][0], forms[f][1]).total > (size_t)kCsMaxSmem) ++f;
+    if (f == 3) return false;
     const int D = forms[f][0], IPS = forms[f][1];
     const CsSmem lay(MT, K, C, D, IPS);
     out->ctas = P;
@@ -378,7 +378,6 @@ static cudaError_t launch_cs(const CsParams& prm, const GemvCsPlan& plan, cudaSt
 template <int MT>
 static cudaError_t launch_cs_mt(const CsParams& prm, const GemvCsPlan& plan, cudaStream_t s, bool pdl) {
     if constexpr (MT <= 2) {
-        if (plan.ips == 4) return launch_cs<MT, 2, 4>(prm, plan, s, pdl);
         if (plan.ips == 2) return launch_cs<MT, 4, 2>(prm, plan, s, pdl);
     }
     return plan.D == 8 ? launch_cs<MT, 8, 1>(prm, plan, s, pdl) : launch_cs<MT, 4, 1>(prm, plan, s, pdl);

@@ -64,7 +64,7 @@ struct GemvCsPlan {
     int ctas;        // one per SM (fewer when the columns are fewer)
     int U, unit;     // column units and their width
     int D;           // ring slots in flight a thread
-    int ips;         // items a slot (4 with D = 2, 2 with D = 4, 1 with D = 8 or 4)
+    int ips;         // items a slot (2 with D = 4, 1 with D = 8 or 4)
     size_t smem;
 };
 bool gemv_cs_plan(int M, int N, int K, int sms, int guH, GemvCsPlan* out);
