@@ -713,6 +713,29 @@ def run_case(case, reps):
     print(json.dumps({"case": case, "reps": reps, "path": path, "ok": True}), flush=True)
 
 
+def run_swa_case(case, reps):
+    """One sliding-window attention call of the swa_decode_attention scenario
+    (Hq = 32, Hkv = 8, d = 128, L = 8448, causal), launched `reps` times back
+    to back (the workload of the attention ncu summary)."""
+    import torch
+    import int4_weight_only_gemm_gb300 as w
+    nq, W = (int(v) for v in case.split(":"))
+    Hq, Hkv, d, L = 32, 8, 128, 8448
+    g = torch.Generator(device="cuda").manual_seed(12)
+    kc = torch.randn((Hkv, L, d), device="cuda", generator=g).to(torch.bfloat16)
+    vt = torch.randn((Hkv, d, L), device="cuda", generator=g).to(torch.bfloat16)
+    q = torch.randn((nq, Hq, d), device="cuda", generator=g).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    ws = w.new_workspace(w.w4a16_swa_workspace_bytes(nq, Hq, Hkv, L, W), "cuda")
+    for _ in range(reps):
+        w.w4a16_swa_attention(q, kc, vt, L, W, False, out=o, workspace=ws)
+    torch.cuda.synchronize()
+    st = w.w4a16_last_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {w.w4a16_status_str(st)}")
+    print(json.dumps({"swa_case": case, "reps": reps, "ok": True}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -725,6 +748,9 @@ def main():
     ap.add_argument("--case", default="",
                     help="SHAPE:M[:PATH] -- run that one GEMM --reps times and exit (for profilers); "
                          "PATH 0 = auto, 1 = split-K GEMV, 2 = tensor-core kernel")
+    ap.add_argument("--swa-case", default="",
+                    help="NQ:W -- run one sliding-window attention call (the swa_decode_attention "
+                         "scenario) --reps times and exit (for profilers)")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--no-sweep", action="store_true", help="skip the M sweep")
     ap.add_argument("--only", default="", help="comma-separated extras to run (default: all)")
@@ -734,6 +760,9 @@ def main():
     args = ap.parse_args()
     if args.case:
         run_case(args.case, args.reps)
+        return
+    if args.swa_case:
+        run_swa_case(args.swa_case, args.reps)
         return
     if args.tune_dispatch:
         ms = tuple(int(v) for v in args.tune_m.split(",")) if args.tune_m else TUNE_M
