@@ -751,6 +751,8 @@ def main():
     ap.add_argument("--swa-case", default="",
                     help="NQ:W -- run one sliding-window attention call (the swa_decode_attention "
                          "scenario) --reps times and exit (for profilers)")
+    ap.add_argument("--requant-case", action="store_true",
+                    help="run the re-quantize + pack of the gate_up weights --reps times and exit (for profilers)")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--no-sweep", action="store_true", help="skip the M sweep")
     ap.add_argument("--only", default="", help="comma-separated extras to run (default: all)")
@@ -763,6 +765,15 @@ def main():
         return
     if args.swa_case:
         run_swa_case(args.swa_case, args.reps)
+        return
+    if args.requant_case:
+        import torch
+        import int4_weight_only_gemm_gb300 as w
+        r = measure_requant(w, torch, "cuda", 1.0, reps=args.reps)
+        st = w.w4a16_last_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {w.w4a16_status_str(st)}")
+        print(json.dumps({"requant_case": r["shape"], "reps": args.reps, "ok": True}), flush=True)
         return
     if args.tune_dispatch:
         ms = tuple(int(v) for v in args.tune_m.split(",")) if args.tune_m else TUNE_M
