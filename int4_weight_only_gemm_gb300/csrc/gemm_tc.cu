@@ -843,8 +843,9 @@ __global__ void __launch_bounds__(TcCfg<NT>::kThreads, 1)
         // Deferred reduction of a split tile by every thread of the CTA: element
         // e of a piece's partials ([NT / 4][128 columns][4 tokens]) is summed
         // over the pieces in piece order, the loads of up to kE elements and
-        // kS pieces in flight at once.
-        constexpr int kE = 3, kS = 8;
+        // kS pieces in flight at once.  kS = 4 rather than 8 (smaller code, run
+        // once per launch): verify step 37.35 -> 37.03 us; kE = 2: 38.54 us.
+        constexpr int kE = 3, kS = 4;
         const int tile = sh_defer[1], ns = sh_defer[2], tokb = sh_defer[3], nbt = sh_defer[4];
         const int W = L.width(nbt);
         const float* base = p.partials + (size_t)tile * ns * NT * 128;
